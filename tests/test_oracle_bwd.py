@@ -1,0 +1,142 @@
+"""Pins of the oracle's backward (Methodology 2, "Quantized Causal Backward",
+of the technical summary of "Hardware-Aware FP4 FlashAttention-4"; FP8
+gradient operands per the arXiv abstract).
+
+mode 1 (identity quantizers) is pinned to the analytic gradient of softmax
+attention and to central finite differences of the brute-force forward;
+mode 0 is pinned by the GQA group-sum identity and by the FP8 error bound on
+inputs whose own views are exactly representable.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from test_oracle_fwd import brute_softmax_attention, rand
+
+
+def analytic_grads(Q, K, V, dO, scale, causal):
+    B, Hq, N, d = Q.shape
+    rep = Hq // K.shape[1]
+    Kr = np.repeat(K.astype(np.float64), rep, 1)
+    Vr = np.repeat(V.astype(np.float64), rep, 1)
+    Q = Q.astype(np.float64)
+    dO = dO.astype(np.float64)
+    S = scale * np.einsum("bhid,bhjd->bhij", Q, Kr)
+    if causal:
+        S = np.where(np.tril(np.ones((N, N), bool)), S, -np.inf)
+    P = np.exp(S - S.max(-1, keepdims=True))
+    P /= P.sum(-1, keepdims=True)
+    O = P @ Vr
+    dV = np.einsum("bhij,bhid->bhjd", P, dO)
+    dP = dO @ Vr.transpose(0, 1, 3, 2)
+    D = (dO * O).sum(-1, keepdims=True)
+    dS = P * (dP - D)
+    dQ = scale * dS @ Kr
+    dK = scale * np.einsum("bhij,bhid->bhjd", dS, Q)
+    sh = (B, K.shape[1], rep, N, d)
+    return dQ, dK.reshape(sh).sum(2), dV.reshape(sh).sum(2)
+
+
+def run_mode1(Q, K, V, dO, causal):
+    d = Q.shape[-1]
+    O, L = brute_softmax_attention(Q, K, V, 1 / np.sqrt(d), causal)
+    return oracle.bwd(Q, K, Q, K, V, O.astype(np.float32), dO, L.astype(np.float32),
+                      causal=causal, mode=1), O, L
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [33, 130])
+def test_mode1_equals_analytic(causal, N):
+    d = 32
+    Q, K, V, dO = rand((1, 4, N, d), 1), rand((1, 2, N, d), 2), rand((1, 2, N, d), 3), rand((1, 4, N, d), 4)
+    # the oracle reads O and LSE as FP32 inputs, so build the reference from
+    # the same rounded O (D = rowsum(dO*O))
+    (dQ, dK, dV), O, L = run_mode1(Q, K, V, dO, causal)
+    aQ, aK, aV = analytic_grads(Q, K, V, dO, 1 / np.sqrt(d), causal)
+    tol = 1e-5    # O and LSE pass through FP32 on their way in
+    np.testing.assert_allclose(dQ, aQ.reshape(-1, d), atol=tol, rtol=0)
+    np.testing.assert_allclose(dK, aK.reshape(-1, d), atol=tol, rtol=0)
+    np.testing.assert_allclose(dV, aV.reshape(-1, d), atol=tol, rtol=0)
+
+
+def test_analytic_matches_finite_differences():
+    """Central differences of f = sum(dO * attention(Q,K,V)) in FP64."""
+    N, d = 20, 16
+    Q, K, V, dO = (rand((1, 2, N, d), s).astype(np.float64) for s in (5, 6, 7, 8))
+    K, V = K[:, :1], V[:, :1]
+    scale = 1 / np.sqrt(d)
+    for causal in (False, True):
+        aQ, aK, aV = analytic_grads(Q, K, V, dO, scale, causal)
+
+        def f(Q_, K_, V_):
+            return float((brute_softmax_attention(Q_, K_, V_, scale, causal)[0] * dO).sum())
+        h = 1e-6
+        rng = np.random.default_rng(0)
+        for _ in range(12):
+            idx = tuple(rng.integers(0, n) for n in (1, 1, N, d))
+            for X, G, which in ((Q, aQ, 0), (K, aK, 1), (V, aV, 2)):
+                iq = (idx[0], rng.integers(0, X.shape[1]), idx[2], idx[3])
+                Xp, Xm = X.copy(), X.copy()
+                Xp[iq] += h
+                Xm[iq] -= h
+                args_p = [Q, K, V]
+                args_m = [Q, K, V]
+                args_p[which], args_m[which] = Xp, Xm
+                fd = (f(*args_p) - f(*args_m)) / (2 * h)
+                assert abs(fd - G[iq]) < 1e-7
+
+
+def quantized_views(Q, K, V, dO):
+    """The method's operands: FP4 Q/K (along d), FP8 column views of Q/K (along
+    N), FP8 row view of V (along d)."""
+    sh_q, sh_k = Q.shape, K.shape
+    Q4 = oracle.dequantize(*oracle.quantize(Q, 0, 0), sh_q, 0, 0)
+    K4 = oracle.dequantize(*oracle.quantize(K, 0, 0), sh_k, 0, 0)
+    Q8 = oracle.dequantize(*oracle.quantize(Q, 1, 1), sh_q, 1, 1)
+    K8 = oracle.dequantize(*oracle.quantize(K, 1, 1), sh_k, 1, 1)
+    V8 = oracle.dequantize(*oracle.quantize(V, 1, 0), sh_k, 1, 0)
+    return Q4, K4, Q8, K8, V8
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_mode0_gqa_is_group_sum(causal):
+    N, d = 100, 32
+    Q, K, V, dO = rand((1, 4, N, d), 9), rand((1, 2, N, d), 10), rand((1, 2, N, d), 11), rand((1, 4, N, d), 12)
+    Q4, K4, Q8, K8, V8 = quantized_views(Q, K, V, dO)
+    O, L = oracle.fwd(Q4, K4, V8, causal=causal)
+    O = O.reshape(Q.shape).astype(np.float32)
+    L = L.reshape(Q.shape[:3]).astype(np.float32)
+    dQ, dK, dV = oracle.bwd(Q4, K4, Q8, K8, V8, O, dO, L, causal=causal)
+    rep = lambda a: np.repeat(a, 2, 1)
+    dQm, dKm, dVm = oracle.bwd(Q4, rep(K4), Q8, rep(K8), rep(V8), O, dO, L, causal=causal)
+    assert np.array_equal(dQ, dQm)
+    dKm = dKm.reshape(1, 2, 2, N, d).sum(2).reshape(-1, d)
+    dVm = dVm.reshape(1, 2, 2, N, d).sum(2).reshape(-1, d)
+    np.testing.assert_allclose(dK, dKm, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dV, dVm, rtol=0, atol=1e-12)
+
+
+def e2m1_exact(shape, seed):
+    """Entries E2M1 values times one power of two per row of 32: exactly
+    representable by every MXFP4 and MXFP8 view."""
+    rng = np.random.default_rng(seed)
+    mags = np.array([0.5, 1, 1.5, 2, 3, 4, 6])
+    return (rng.choice(mags, shape) * rng.choice([-1.0, 1.0], shape) * 0.25).astype(np.float32)
+
+
+def test_mode0_within_fp8_bound():
+    """On inputs whose FP4/FP8 views are exact, mode 0 differs from mode 1
+    only by the E4M3 rounding of P, dS and the dO views (half-ulp 2^-4
+    relative per element), so the relative L2 gap stays a few percent."""
+    N, d = 96, 32
+    Q, K = e2m1_exact((1, 2, N, d), 1), e2m1_exact((1, 2, N, d), 2)
+    V, dO = e2m1_exact((1, 2, N, d), 3), e2m1_exact((1, 2, N, d), 4)
+    Q4, K4, Q8, K8, V8 = quantized_views(Q, K, V, dO)
+    assert np.array_equal(Q4, Q) and np.array_equal(Q8, Q) and np.array_equal(V8, V)
+    O, L = brute_softmax_attention(Q, K, V, 1 / np.sqrt(d), True)
+    O, L = O.astype(np.float32), L.astype(np.float32)
+    g0 = oracle.bwd(Q, K, Q, K, V, O, dO, L, causal=True, mode=0)
+    g1 = oracle.bwd(Q, K, Q, K, V, O, dO, L, causal=True, mode=1)
+    for a, b in zip(g0, g1):
+        rel = np.linalg.norm(a - b) / np.linalg.norm(b)
+        assert 1e-4 < rel < 0.06

@@ -1,0 +1,171 @@
+"""Pins of the oracle's element formats and block quantization.
+
+Each check compares the oracle with something other than itself: the format
+definitions (bit fields), a library conversion (torch float8_e4m3fn), an
+independent binade-wise round-half-even, or an invariant of the OCP MX rule.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+E2M1_MAGS = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]   # E2M1 (bias 1, 1 mantissa bit)
+
+
+def test_e2m1_table_and_roundtrip():
+    for c in range(16):
+        v = oracle.e2m1_value(c)
+        mag = E2M1_MAGS[c & 7]
+        assert abs(v) == mag
+        assert np.signbit(v) == bool(c & 8)
+        assert oracle.round_to_code(v, 0) == c        # every code re-encodes to itself
+    assert oracle.round_to_code(-0.0, 0) == 0x8       # negative zero keeps its sign
+
+
+def test_e4m3_table_matches_torch():
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ours = np.array([oracle.e4m3_value(c) for c in range(256)])
+    nan = np.isnan(lib)
+    assert np.array_equal(nan, np.isnan(ours))
+    assert nan.sum() == 2 and nan[0x7F] and nan[0xFF]
+    assert np.array_equal(lib[~nan], ours[~nan])
+    assert np.array_equal(np.signbit(lib[~nan]), np.signbit(ours[~nan]))
+    for c in range(256):
+        if c in (0x7F, 0xFF):
+            continue
+        assert oracle.round_to_code(oracle.e4m3_value(c), 1) == c
+    assert oracle.e4m3_value(0x7E) == 448.0 and oracle.e4m3_value(1) == 2.0 ** -9
+
+
+def test_e8m0():
+    for b in range(255):
+        assert oracle.e8m0_value(b) == 2.0 ** (b - 127)
+    assert np.isnan(oracle.e8m0_value(255))
+
+
+# ---------------------------------------------------------------------------
+# independent rounding: round-half-even per binade (numpy rint), saturating
+# ---------------------------------------------------------------------------
+
+def rne_e2m1(y: np.ndarray) -> np.ndarray:
+    a = np.abs(y)
+    q = np.where(a < 2, np.rint(a * 2) / 2, np.where(a < 4, np.rint(a), 2 * np.rint(a / 2)))
+    return np.copysign(np.minimum(q, 6.0), y)
+
+
+def rne_e4m3(y: np.ndarray) -> np.ndarray:
+    a = np.abs(y)
+    _, e = np.frexp(a)                       # a = f * 2^e, f in [0.5, 1)
+    e = np.maximum(e - 1, -6)                # binade exponent, subnormals share -6
+    step = np.ldexp(1.0, e - 3)
+    q = np.rint(a / step) * step
+    return np.copysign(np.minimum(q, 448.0), y)
+
+
+def all_finite_bf16() -> np.ndarray:
+    bits = np.arange(65536, dtype=np.uint32) << 16
+    v = bits.view(np.float32)
+    return v[np.isfinite(v)]
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("X", [-127, -40, -3, 0, 7, 100, 117])
+def test_quantize_exhaustive_bf16(fmt, X):
+    """All finite bf16 values that keep the block exponent at X, each in a
+    block whose amax is pinned by an anchor 2^(X+emax)."""
+    emax = 2 if fmt == 0 else 8
+    if X + emax > 127:
+        pytest.skip("anchor not representable")
+    anchor = np.float32(np.ldexp(1.0, X + emax))
+    v = all_finite_bf16()
+    v = v[np.abs(v.astype(np.float64)) < 2.0 * float(anchor)]
+    nblk = -(-v.size // 31)
+    pad = np.zeros(nblk * 31, dtype=np.float32)
+    pad[: v.size] = v
+    x = np.concatenate([np.full((nblk, 1), anchor, np.float32), pad.reshape(nblk, 31)], axis=1)
+    x = x.reshape(1, 1, nblk, 32)
+    codes, scales = oracle.quantize(x, fmt, oracle.ALONG_D)
+    assert np.all(scales == X + 127)
+    deq = oracle.dequantize(codes, scales, x.shape, fmt, oracle.ALONG_D).astype(np.float64)
+    y = np.ldexp(x.astype(np.float64), -X)
+    want = (rne_e2m1(y) if fmt == 0 else rne_e4m3(y)) * np.ldexp(1.0, X)
+    assert np.array_equal(deq, want)
+    assert np.array_equal(np.signbit(deq), np.signbit(want))
+
+
+def test_e4m3_rounding_matches_torch_in_range():
+    g = torch.Generator().manual_seed(3)
+    y = (torch.rand(200000, generator=g, dtype=torch.float64) * 2 - 1) * 460
+    y = y.to(torch.float32)
+    lib = y.to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ok = np.abs(y.numpy()) <= 448
+    ours = np.array([oracle.e4m3_value(oracle.round_to_code(float(t), 1)) for t in y.numpy()[ok][:20000]])
+    assert np.array_equal(ours, lib[ok][:20000])
+
+
+@pytest.mark.parametrize("fmt,lo,hi", [(0, 4.0, 8.0), (1, 256.0, 512.0)])
+def test_block_exponent_closed_form(fmt, lo, hi):
+    g = np.random.default_rng(0)
+    a = np.float32(np.abs(g.standard_normal(5000)) * np.exp2(g.integers(-60, 60, 5000))) + np.float32(1e-30)
+    for amax in a:
+        X = oracle.block_exponent(float(amax), fmt)
+        r = float(amax) * 2.0 ** -X
+        assert lo <= r < hi
+    assert oracle.block_exponent(0.0, fmt) == -127
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("axis", [0, 1])
+def test_quantize_scale_and_sign_invariants(fmt, axis):
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(2, 3, 77, 64, generator=g).to(torch.bfloat16).float().numpy()
+    c0, s0 = oracle.quantize(x, fmt, axis)
+    for k in (-5, 1, 9):
+        c1, s1 = oracle.quantize(np.ldexp(x, k).astype(np.float32), fmt, axis)
+        assert np.array_equal(c1, c0)
+        valid = s0 > 0    # all-zero padding blocks are clamped at -127
+        assert np.array_equal(s1[valid].astype(int), s0[valid].astype(int) + k)
+    cn, sn = oracle.quantize(-x, fmt, axis)
+    flip = 0x88 if fmt == 0 else 0x80
+    if axis == 1:
+        # padded positions hold +0 on both sides
+        Np = oracle.padded_n(x.shape[2])
+        mask = np.zeros(c0.shape, dtype=np.uint8)
+        per = 2 if fmt == 0 else 1
+        cols = x.shape[2] // per
+        mask[..., :cols] = flip
+        if fmt == 0 and x.shape[2] % 2:
+            mask[..., cols] = 0x08
+        assert Np > x.shape[2]
+        assert np.array_equal(cn, c0 ^ mask)
+    else:
+        assert np.array_equal(cn, c0 ^ flip)
+    assert np.array_equal(sn, s0)
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_along_n_is_along_d_of_the_transpose(fmt):
+    """Quantizing along N equals quantizing the zero-padded transpose along d."""
+    g = torch.Generator().manual_seed(7)
+    B, H, N, d = 1, 2, 200, 64
+    x = torch.randn(B, H, N, d, generator=g).to(torch.bfloat16).float().numpy()
+    cN, sN = oracle.quantize(x, fmt, oracle.ALONG_N)
+    Np = oracle.padded_n(N)
+    xt = np.zeros((B, H, d, Np), dtype=np.float32)
+    xt[:, :, :, :N] = np.swapaxes(x, 2, 3)
+    cD, sD = oracle.quantize(xt, fmt, oracle.ALONG_D)
+    assert np.array_equal(cN, cD) and np.array_equal(sN, sD)
+    back = oracle.dequantize(cN, sN, x.shape, fmt, oracle.ALONG_N)
+    want = np.swapaxes(oracle.dequantize(cD, sD, xt.shape, fmt, oracle.ALONG_D), 2, 3)[:, :, :N]
+    assert np.array_equal(back, want)
+
+
+def test_nibble_order():
+    """Element 2i sits in the low nibble, 2i+1 in the high nibble."""
+    x = np.zeros((1, 1, 1, 32), dtype=np.float32)
+    x[0, 0, 0, 0] = 4.0      # amax 4 -> X = 0
+    x[0, 0, 0, 1] = 0.5
+    codes, scales = oracle.quantize(x, 0, oracle.ALONG_D)
+    assert scales[0, 0, 0, 0] == 127
+    assert codes[0, 0, 0, 0] == (0x6 | (0x1 << 4))

@@ -1,0 +1,169 @@
+"""Pins of the oracle's tiled forward (Methodology 1 of the technical summary
+of "Hardware-Aware FP4 FlashAttention-4").
+
+mode 1 (exact exponentials, identity quantizers) is pinned to brute-force
+softmax attention in numpy; mode 0 (Direct-P) to closed-form limits and
+invariants that hold for the method exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+
+def brute_softmax_attention(Q, K, V, scale, causal):
+    """Textbook softmax(scale*QK^T)V in FP64, K/V heads repeated for GQA."""
+    B, Hq, N, d = Q.shape
+    rep = Hq // K.shape[1]
+    K = np.repeat(K.astype(np.float64), rep, axis=1)
+    V = np.repeat(V.astype(np.float64), rep, axis=1)
+    S = scale * np.einsum("bhid,bhjd->bhij", Q.astype(np.float64), K)
+    if causal:
+        S = np.where(np.tril(np.ones((N, N), bool)), S, -np.inf)
+    mx = S.max(-1, keepdims=True)
+    P = np.exp(S - mx)
+    l = P.sum(-1, keepdims=True)
+    return np.einsum("bhij,bhjd->bhid", P / l, V), (mx + np.log(l))[..., 0]
+
+
+def rand(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * scale).to(torch.bfloat16).float().numpy()
+
+
+@pytest.mark.parametrize("N", [1, 5, 127, 128, 129, 300])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hq,Hkv", [(2, 2), (4, 2)])
+def test_mode1_equals_brute_force(N, causal, Hq, Hkv):
+    d = 64
+    Q, K, V = rand((1, Hq, N, d), 1), rand((1, Hkv, N, d), 2), rand((1, Hkv, N, d), 3)
+    O, L = oracle.fwd(Q, K, V, causal=causal, mode=1)
+    Ob, Lb = brute_softmax_attention(Q, K, V, 1 / np.sqrt(d), causal)
+    np.testing.assert_allclose(O, Ob.reshape(-1, d), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(L, Lb.reshape(-1), rtol=0, atol=1e-12)
+
+
+def quantized_inputs(Q, K, V):
+    shp_q, shp_k = Q.shape, K.shape
+    qc, qs = oracle.quantize(Q, 0, oracle.ALONG_D)
+    kc, ks = oracle.quantize(K, 0, oracle.ALONG_D)
+    vc, vs = oracle.quantize(V, 0, oracle.ALONG_N)
+    return (oracle.dequantize(qc, qs, shp_q, 0, oracle.ALONG_D),
+            oracle.dequantize(kc, ks, shp_k, 0, oracle.ALONG_D),
+            oracle.dequantize(vc, vs, shp_k, 0, oracle.ALONG_N))
+
+
+def test_hard_attention_limit_and_ties():
+    """If each row's max score beats every other by more than ln(24)/scale
+    (and the max sits in the first key tile), every other key gets code 0 and
+    O_i is exactly the argmax key's V row; two tied maxima give their mean."""
+    d, N = 64, 300
+    rng = np.random.default_rng(0)
+    K = np.zeros((1, 1, N, d), np.float32)
+    K[0, 0] = np.sign(rng.standard_normal((N, d))) * 0.5        # E2M1-exact entries
+    Q = np.zeros((1, 1, 64, d), np.float32)
+    targets = rng.integers(0, 128, 64)
+    Q[0, 0] = 4.0 * K[0, 0, targets]                            # q.k_target = 4*d*0.25 = 64
+    V = rand((1, 1, N, d), 9)
+    Qd, Kd, Vd = quantized_inputs(np.concatenate([Q, np.zeros((1, 1, N - 64, d), np.float32)], 2), K, V)
+    scale = 1 / np.sqrt(d)
+    S = Qd[0, 0, :64] @ Kd[0, 0].T
+    top2 = np.sort(S, axis=1)[:, -2:]
+    assert np.all(scale * (top2[:, 1] - top2[:, 0]) > np.log(24) + 0.01)
+    O, _ = oracle.fwd(Qd, Kd, Vd, rows=np.arange(64))
+    assert np.array_equal(O, Vd[0, 0, targets].astype(np.float64))
+    # tie: duplicate the target key of row 0 into key 7 (tile 0)
+    K2 = Kd.copy()
+    K2[0, 0, 7] = K2[0, 0, targets[0]]
+    if targets[0] != 7:
+        O2, _ = oracle.fwd(Qd, K2, Vd, rows=np.arange(1))
+        want = (Vd[0, 0, targets[0]].astype(np.float64) + Vd[0, 0, 7]) / 2
+        np.testing.assert_allclose(O2[0], want, rtol=0, atol=1e-15)
+
+
+def test_permutation_within_tile_invariance():
+    d, N = 64, 300
+    Qd, Kd, Vd = quantized_inputs(rand((1, 2, N, d), 4), rand((1, 2, N, d), 5), rand((1, 2, N, d), 6))
+    O, L = oracle.fwd(Qd, Kd, Vd)
+    rng = np.random.default_rng(1)
+    perm = np.concatenate([rng.permutation(np.arange(t, min(N, t + 128))) for t in range(0, N, 128)])
+    Op, Lp = oracle.fwd(Qd, Kd[:, :, perm], Vd[:, :, perm])
+    np.testing.assert_allclose(Op, O, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(Lp, L, rtol=0, atol=1e-12)
+
+
+def test_any_permutation_when_max_in_first_tile():
+    """With Q >= 0 and a dominant positive key 0, every row's max is in tile 0,
+    every code is taken against the final max, and key order is irrelevant."""
+    d, N = 64, 384
+    rng = np.random.default_rng(2)
+    Q = np.abs(rand((1, 1, N, d), 7))
+    K = rand((1, 1, N, d), 8) * 0.25
+    K[0, 0, 0] = 2.0
+    Qd, Kd, Vd = quantized_inputs(Q, K, rand((1, 1, N, d), 9))
+    O, L = oracle.fwd(Qd, Kd, Vd)
+    perm = np.concatenate([[0], 1 + rng.permutation(N - 1)])
+    Op, Lp = oracle.fwd(Qd, Kd[:, :, perm], Vd[:, :, perm])
+    np.testing.assert_allclose(Op, O, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(Lp, L, rtol=0, atol=1e-12)
+    # and the tiled result equals Direct-P against the global max (brute force)
+    c = np.float32(np.float32(1 / np.sqrt(d)) * np.float32(np.log2(np.e)))
+    S = (Qd[0, 0].astype(np.float64) @ Kd[0, 0].T.astype(np.float64)).astype(np.float32)
+    m = S.max(1, keepdims=True)
+    codes = np.array([[oracle.directp_code(float(s), float(mm), float(c)) for s in row]
+                      for row, mm in zip(S[:8], m[:8, 0])])
+    vals = np.array([0, .5, 1, 1.5, 2, 3, 4, 6])[codes]
+    want = vals @ Vd[0, 0].astype(np.float64) / vals.sum(1, keepdims=True)
+    np.testing.assert_allclose(O[:8], want, rtol=0, atol=1e-12)
+
+
+def test_constant_v():
+    d, N = 64, 300
+    v = np.array([0.5, -1.0, 3.0, 0.0] * (d // 4), np.float32)
+    V = np.broadcast_to(v, (1, 2, N, d)).copy()
+    Qd, Kd, Vd = quantized_inputs(rand((1, 2, N, d), 10, 2.0), rand((1, 2, N, d), 11, 2.0), V)
+    assert np.array_equal(Vd[0, 0, 0], v)
+    O, L = oracle.fwd(Qd, Kd, Vd)
+    np.testing.assert_allclose(O, np.broadcast_to(v, O.shape), rtol=0, atol=1e-6)
+    # l >= 6 (the running max's key carries code 7) -> LSE >= scale * max s
+    S = np.einsum("bhid,bhjd->bhij", Qd.astype(np.float64), Kd.astype(np.float64))
+    assert np.all(L >= (S.max(-1).reshape(-1) / np.sqrt(d)) - 1e-9)
+
+
+def test_causal_first_row_and_future_independence():
+    d, N = 64, 260
+    Qd, Kd, Vd = quantized_inputs(rand((1, 1, N, d), 12), rand((1, 1, N, d), 13), rand((1, 1, N, d), 14))
+    O, _ = oracle.fwd(Qd, Kd, Vd, causal=True)
+    assert np.array_equal(O[0], Vd[0, 0, 0].astype(np.float64))
+    i = 140
+    K2, V2 = Kd.copy(), Vd.copy()
+    K2[:, :, i + 1:] = rand((1, 1, N - i - 1, d), 15)
+    V2[:, :, i + 1:] = rand((1, 1, N - i - 1, d), 16)
+    O2, _ = oracle.fwd(Qd, K2, V2, causal=True, rows=np.arange(i + 1))
+    assert np.array_equal(O2, O[: i + 1])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_equals_repeated_mha(causal):
+    d, N = 64, 200
+    Qd, Kd, Vd = quantized_inputs(rand((2, 4, N, d), 17), rand((2, 2, N, d), 18), rand((2, 2, N, d), 19))
+    O, L = oracle.fwd(Qd, Kd, Vd, causal=causal)
+    Om, Lm = oracle.fwd(Qd, np.repeat(Kd, 2, 1), np.repeat(Vd, 2, 1), causal=causal)
+    assert np.array_equal(O, Om) and np.array_equal(L, Lm)
+
+
+def test_directp_close_to_softmax():
+    """Direct-P is an approximation of softmax: its LSE is within the E2M1
+    quantization error of the exact one (which also pins the l/6 factor), and
+    its output stays well correlated with exact attention."""
+    d, N = 64, 256
+    Q, K, V = rand((1, 2, N, d), 20), rand((1, 2, N, d), 21), rand((1, 2, N, d), 22)
+    Qd, Kd, Vd = quantized_inputs(Q, K, V)
+    O, L = oracle.fwd(Qd, Kd, Vd)
+    O1, L1 = oracle.fwd(Qd, Kd, Vd, mode=1)
+    # E2M1 drops keys below 1/24 of the running max, so l/6 under-counts the
+    # exact mass a little; a missing or doubled factor 6 would be off by ln 6.
+    assert np.max(np.abs(L - L1)) < 0.9 and np.mean(np.abs(L - L1)) < 0.2
+    cos = np.sum(O * O1, 1) / np.linalg.norm(O, axis=1) / np.linalg.norm(O1, axis=1)
+    assert cos.mean() > 0.9
