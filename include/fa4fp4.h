@@ -1,0 +1,155 @@
+/*
+ * fa4fp4.h -- C ABI of the GB300 (sm_103a) block-scaled FP4 attention library
+ * with Direct-P.
+ *
+ * The method is the one described in "Hardware-Aware FP4 FlashAttention-4"
+ * (arXiv:2609.04105; gist.science technical summary and the arXiv abstract):
+ * Q and K quantized to E2M1 with power-of-two (E8M0) scales per 32 elements,
+ * S = Q K^T on FP4 tensor cores, each score's offset from the running row max
+ * mapped straight to an E2M1 probability code, P V on FP4 tensor cores with an
+ * online-softmax rescale of O, and a causal backward that rebuilds P from the
+ * saved quantized Q and K and uses FP8 E4M3 operands.
+ *
+ * Conventions shared by every call:
+ *   - Pointers are DEVICE pointers, allocated and owned by the caller.  The
+ *     library never allocates or frees memory and never synchronizes, except
+ *     in fa4fp4_sync_status.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every compute call is asynchronous on it; the return value
+ *     reports host-side argument validation and launch errors only.  Device
+ *     watchdog errors (a pipeline wait that ran out of time) are reported by
+ *     fa4fp4_sync_status.
+ *   - Tensors are dense and row-major in the layouts stated below; every
+ *     pointer must be 16-byte aligned (FA4FP4_ERR_ALIGNMENT otherwise).
+ *   - Supported shapes: d in {64, 128}; N >= 1; B, H >= 0 (0 is a no-op);
+ *     Hq % Hkv == 0; causal attention uses the same N for queries and keys,
+ *     aligned top-left (key n is visible to query i iff n <= i).
+ *   - softmax_scale <= 0 selects 1/sqrt(d).
+ *   - No C++ exception crosses this boundary; there is no CPU fallback.
+ *
+ * Quantized tensor layouts ("qtensor": a codes buffer plus a scales buffer):
+ *   blocks along d (FA4FP4_BLOCKS_ALONG_D), logical x[B][H][N][d]:
+ *       codes  [B][H][N][d/2] bytes (MXFP4: two E2M1 codes per byte, element
+ *              2i in the low nibble) or [B][H][N][d] bytes (MXFP8: E4M3)
+ *       scales [B][H][N][d/32] E8M0 bytes
+ *   blocks along N (FA4FP4_BLOCKS_ALONG_N), stored transposed, Np = N rounded
+ *   up to a multiple of 128, positions >= N hold +0:
+ *       codes  [B][H][d][Np/2] (MXFP4) or [B][H][d][Np] (MXFP8)
+ *       scales [B][H][d][Np/32]
+ */
+#ifndef FA4FP4_H
+#define FA4FP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FA4FP4_API __attribute__((visibility("default")))
+#else
+#define FA4FP4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA4FP4_OK = 0,
+  FA4FP4_ERR_INVALID_ARG = 1,    /* null pointer, negative size, bad enum */
+  FA4FP4_ERR_UNSUPPORTED = 2,    /* d not in {64,128}, Hq % Hkv != 0, ... */
+  FA4FP4_ERR_ALIGNMENT = 3,      /* a pointer is not 16-byte aligned */
+  FA4FP4_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed */
+  FA4FP4_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait expired */
+  FA4FP4_ERR_WORKSPACE = 6       /* workspace missing or too small */
+} fa4fp4_status;
+
+typedef enum { FA4FP4_FMT_MXFP4 = 0, FA4FP4_FMT_MXFP8_E4M3 = 1 } fa4fp4_format;
+typedef enum { FA4FP4_BLOCKS_ALONG_D = 0, FA4FP4_BLOCKS_ALONG_N = 1 } fa4fp4_axis;
+typedef enum { FA4FP4_OUT_F32 = 0, FA4FP4_OUT_BF16 = 1 } fa4fp4_out_dtype;
+
+/* Bytes of the codes buffer of a quantized tensor; *scale_bytes (if not NULL)
+ * receives the bytes of its scales buffer.  Returns 0 for invalid arguments. */
+FA4FP4_API size_t fa4fp4_qtensor_bytes(int B, int H, int N, int d, int fmt, int axis, size_t* scale_bytes);
+
+/* Block quantization (technical summary, Methodology 1 "Format Selection";
+ * Methodology 2 "Gradient Formats").  x_bf16 is [B][H][N][d] bf16.  Each block
+ * of 32 elements along `axis` gets the E8M0 exponent X = floor(log2(amax)) -
+ * emax (emax 2 for E2M1, 8 for E4M3; OCP MX rule; clamped to [-127,127]); each
+ * element is x * 2^-X rounded to nearest-even on the element grid, saturating,
+ * with its sign kept.  Writes codes/scales in the layouts above. */
+FA4FP4_API fa4fp4_status fa4fp4_quantize(const void* x_bf16, int B, int H, int N, int d, int fmt, int axis,
+                              void* codes, void* scales, void* stream);
+
+/* Direct-P forward (technical summary, Methodology 1 "Direct Mapping" and
+ * "Consistent Normalization"; abstract).
+ *   q: MXFP4 along d, [B][Hq][N][d];  k: MXFP4 along d, [B][Hkv][N][d];
+ *   vt: MXFP4 along N (transposed V), [B][Hkv][d][Np].
+ *   Query head h reads kv head h / (Hq/Hkv).
+ * Per 128-query tile, key tiles of 128 are visited in ascending order; for
+ * key tile j the running max m_j = max(m_{j-1}, row max of S_j); each score s
+ * gets the E2M1 code #{k : fmaf(s, c, -fl32(m_j*c)) >= T_k}, c =
+ * fl32(softmax_scale*log2 e), T_k the smallest FP32 x with RNE_E2M1(6*2^x) >=
+ * the k-th E2M1 magnitude; P blocks carry the unit E8M0 scale; O and the
+ * normalizer l are rescaled by 2^(c(m_{j-1}-m_j)) before P_j V_j is added and
+ * l accumulates the same code values.  Output o = O/l ([B][Hq][N][d], f32 or
+ * bf16 per out_dtype) and, if lse != NULL, lse[B][Hq][N] = softmax_scale*m +
+ * ln(l/6) (f32). */
+FA4FP4_API fa4fp4_status fa4fp4_fwd(const void* q_codes, const void* q_scales, const void* k_codes,
+                         const void* k_scales, const void* vt_codes, const void* vt_scales,
+                         int B, int Hq, int Hkv, int N, int d, float softmax_scale, int causal,
+                         void* o, int out_dtype, float* lse, void* stream);
+
+/* Bytes of caller-provided workspace fa4fp4_bwd needs. */
+FA4FP4_API size_t fa4fp4_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
+
+/* Quantized causal backward (technical summary, Methodology 2 "Quantized
+ * Causal Backward": P rebuilt from the saved quantized Q/K and the LSE;
+ * row/column FP8 views of Q, K, V; abstract: FP8 gradient operands).
+ *   q4, k4: the forward's MXFP4 Q/K (along d);
+ *   q8c, k8c: MXFP8 Q/K blocked along N ([B][H][d][Np] transposed views);
+ *   v8r: MXFP8 V blocked along d ([B][Hkv][N][d]);
+ *   o: forward output [B][Hq][N][d] (f32 or bf16 per o_dtype);
+ *   dout: upstream gradient, bf16 [B][Hq][N][d];  lse: f32 [B][Hq][N].
+ * Computes P = 2^(fmaf(s, c, -fl32(lse*log2 e))), D = rowsum(dO*O), the MXFP8
+ * views of dO (blocks along d and blocks of 32 queries), dP = dO V^T, dS =
+ * P*(dP-D), and, with P and dS quantized to MXFP8 (P and dS in blocks of 32
+ * queries for dV/dK, dS in blocks of 32 keys for dQ):
+ *   dV = P^T dO, dK = scale * dS^T Q, dQ = scale * dS K
+ * summed over the query heads of each kv head.  dq [B][Hq][N][d], dk/dv
+ * [B][Hkv][N][d], all f32, fully overwritten.  `workspace` must hold
+ * fa4fp4_bwd_workspace_bytes(...) bytes (FA4FP4_ERR_WORKSPACE otherwise). */
+FA4FP4_API fa4fp4_status fa4fp4_bwd(const void* q4_codes, const void* q4_scales, const void* k4_codes,
+                         const void* k4_scales, const void* q8c_codes, const void* q8c_scales,
+                         const void* k8c_codes, const void* k8c_scales, const void* v8r_codes,
+                         const void* v8r_scales, const void* o, int o_dtype, const void* dout,
+                         const float* lse, int B, int Hq, int Hkv, int N, int d,
+                         float softmax_scale, int causal, float* dq, float* dk, float* dv,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* BF16 FlashAttention forward, the speedup reference for fa4fp4_fwd
+ * (technical summary, Results: "HAO's BF16 baseline").  q [B][Hq][N][d], k/v
+ * [B][Hkv][N][d] bf16; exact online softmax with P rounded to bf16 for the
+ * P V product.  o as in fa4fp4_fwd; lse (nullable) = natural-log LSE. */
+FA4FP4_API fa4fp4_status fa4bf16_fwd(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,
+                          int N, int d, float softmax_scale, int causal, void* o, int out_dtype,
+                          float* lse, void* stream);
+
+/* Direct-P code map on its own: codes[i] = #{k : fmaf(s[i], c, -fl32(m*c)) >=
+ * T_k} for n scores (device arrays; codes one byte each).  Uses the same
+ * device classifier as fa4fp4_fwd. */
+FA4FP4_API fa4fp4_status fa4fp4_directp_codes(const float* s, int64_t n, float m, float c, uint8_t* codes,
+                                   void* stream);
+
+/* Synchronizes `stream`, then returns FA4FP4_ERR_CUDA for a pending CUDA error
+ * or FA4FP4_ERR_DEVICE_TIMEOUT if any kernel's bounded wait expired since the
+ * last call (the flag is cleared), else FA4FP4_OK. */
+FA4FP4_API fa4fp4_status fa4fp4_sync_status(void* stream);
+
+/* Static description of a status code. */
+FA4FP4_API const char* fa4fp4_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA4FP4_H */

@@ -7,13 +7,12 @@ built library is missing.  There is no CPU fallback.
 """
 from .inputs import Workload, make_inputs  # noqa: F401  (no CUDA needed)
 
-_API = ("quantize", "fwd", "bwd", "bf16_fwd", "qtensor_alloc", "sync_status", "library_path",
-        "load_library", "FMT_MXFP4", "FMT_MXFP8", "ALONG_D", "ALONG_N", "OUT_F32", "OUT_BF16",
-        "QTensor", "Fa4Fp4Error")
-
-
 def __getattr__(name):
-    if name in _API:
-        from . import api
+    if name.startswith("__"):
+        raise AttributeError(name)
+    import importlib
+    api = importlib.import_module(__name__ + ".api")
+    try:
         return getattr(api, name)
-    raise AttributeError(name)
+    except AttributeError:
+        raise AttributeError(name) from None

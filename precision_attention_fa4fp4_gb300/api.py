@@ -1,0 +1,205 @@
+"""Thin ctypes binding of the C ABI in include/fa4fp4.h.
+
+Argument marshalling only: torch tensors give device pointers and the current
+stream; every step of the computation runs in the CUDA library.  If the
+library is not built, or is called on tensors that are not on a CUDA device,
+the call raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(HERE, "libfa4fp4.so")
+
+FMT_MXFP4, FMT_MXFP8 = 0, 1
+ALONG_D, ALONG_N = 0, 1
+OUT_F32, OUT_BF16 = 0, 1
+_STATUS_OK = 0
+
+
+class Fa4Fp4Error(RuntimeError):
+    def __init__(self, where: str, status: int):
+        msg = library().fa4fp4_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{where}: {msg} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libfa4fp4.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {_LIB_PATH} (run __graft_entry__.build())")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.fa4fp4_status_string.restype = ctypes.c_char_p
+        lib.fa4fp4_status_string.argtypes = [i]
+        lib.fa4fp4_qtensor_bytes.restype = sz
+        lib.fa4fp4_qtensor_bytes.argtypes = [i, i, i, i, i, i, ctypes.POINTER(sz)]
+        lib.fa4fp4_quantize.restype = i
+        lib.fa4fp4_quantize.argtypes = [vp, i, i, i, i, i, i, vp, vp, vp]
+        lib.fa4fp4_fwd.restype = i
+        lib.fa4fp4_fwd.argtypes = [vp] * 6 + [i, i, i, i, i, f, i, vp, i, vp, vp]
+        lib.fa4fp4_bwd_workspace_bytes.restype = sz
+        lib.fa4fp4_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
+        lib.fa4fp4_bwd.restype = i
+        lib.fa4fp4_bwd.argtypes = [vp] * 11 + [i, vp, vp, i, i, i, i, i, f, i, vp, vp, vp, vp, sz, vp]
+        lib.fa4bf16_fwd.restype = i
+        lib.fa4bf16_fwd.argtypes = [vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, vp]
+        lib.fa4fp4_directp_codes.restype = i
+        lib.fa4fp4_directp_codes.argtypes = [vp, ctypes.c_int64, f, f, vp, vp]
+        lib.fa4fp4_sync_status.restype = i
+        lib.fa4fp4_sync_status.argtypes = [vp]
+        _lib = lib
+    return _lib
+
+
+def library():
+    return load_library()
+
+
+def _check(where: str, status: int):
+    if status != _STATUS_OK:
+        raise Fa4Fp4Error(where, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device=None):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("fa4fp4: tensors must be contiguous CUDA tensors")
+
+
+def padded_n(N: int) -> int:
+    return (N + 127) // 128 * 128
+
+
+@dataclass
+class QTensor:
+    """A block-quantized tensor: codes + E8M0 scales in the canonical layout
+    of include/fa4fp4.h, logical shape (B, H, N, d)."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+    shape: tuple
+    fmt: int
+    axis: int
+
+
+def qtensor_shapes(B, H, N, d, fmt, axis):
+    L, R = (d, N) if axis == ALONG_D else (padded_n(N), d)
+    per = L // 2 if fmt == FMT_MXFP4 else L
+    return (B, H, R, per), (B, H, R, L // 32)
+
+
+def qtensor_alloc(B, H, N, d, fmt, axis, device="cuda") -> QTensor:
+    cs, ss = qtensor_shapes(B, H, N, d, fmt, axis)
+    return QTensor(torch.empty(cs, dtype=torch.uint8, device=device),
+                   torch.empty(ss, dtype=torch.uint8, device=device), (B, H, N, d), fmt, axis)
+
+
+def quantize(x: torch.Tensor, fmt: int = FMT_MXFP4, axis: int = ALONG_D, out: QTensor | None = None) -> QTensor:
+    """Block-quantize a bf16 [B,H,N,d] CUDA tensor (fa4fp4_quantize)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 4:
+        raise ValueError("quantize expects a bf16 [B,H,N,d] tensor")
+    _cuda(x)
+    B, H, N, d = x.shape
+    q = out if out is not None else qtensor_alloc(B, H, N, d, fmt, axis, x.device)
+    _check("fa4fp4_quantize", load_library().fa4fp4_quantize(
+        _ptr(x), B, H, N, d, fmt, axis, _ptr(q.codes), _ptr(q.scales), _stream(x.device)))
+    return q
+
+
+def fwd(q: QTensor, k: QTensor, vt: QTensor, causal: bool = False, softmax_scale: float = 0.0,
+        out_dtype: int = OUT_BF16, with_lse: bool = True, out=None, lse=None):
+    """Direct-P FP4 forward (fa4fp4_fwd).  Returns (o, lse or None)."""
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    dev = q.codes.device
+    if out is None:
+        out = torch.empty((B, Hq, N, d), dtype=torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32, device=dev)
+    if with_lse and lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    _cuda(q.codes, q.scales, k.codes, k.scales, vt.codes, vt.scales, out, lse)
+    _check("fa4fp4_fwd", load_library().fa4fp4_fwd(
+        _ptr(q.codes), _ptr(q.scales), _ptr(k.codes), _ptr(k.scales), _ptr(vt.codes), _ptr(vt.scales),
+        B, Hq, Hkv, N, d, float(softmax_scale), int(bool(causal)), _ptr(out), out_dtype,
+        _ptr(lse) if with_lse else None, _stream(dev)))
+    return out, (lse if with_lse else None)
+
+
+def bwd_workspace_bytes(B, Hq, Hkv, N, d) -> int:
+    return int(load_library().fa4fp4_bwd_workspace_bytes(B, Hq, Hkv, N, d))
+
+
+def bwd(q4: QTensor, k4: QTensor, q8c: QTensor, k8c: QTensor, v8r: QTensor, o: torch.Tensor,
+        dout: torch.Tensor, lse: torch.Tensor, causal: bool = True, softmax_scale: float = 0.0,
+        workspace: torch.Tensor | None = None):
+    """Quantized backward (fa4fp4_bwd).  Returns (dq, dk, dv) in float32."""
+    B, Hq, N, d = q4.shape
+    Hkv = k4.shape[1]
+    dev = dout.device
+    dq = torch.empty((B, Hq, N, d), dtype=torch.float32, device=dev)
+    dk = torch.empty((B, Hkv, N, d), dtype=torch.float32, device=dev)
+    dv = torch.empty((B, Hkv, N, d), dtype=torch.float32, device=dev)
+    ws_bytes = bwd_workspace_bytes(B, Hq, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    o_dtype = OUT_BF16 if o.dtype == torch.bfloat16 else OUT_F32
+    _cuda(o, dout, lse, workspace)
+    _check("fa4fp4_bwd", load_library().fa4fp4_bwd(
+        _ptr(q4.codes), _ptr(q4.scales), _ptr(k4.codes), _ptr(k4.scales), _ptr(q8c.codes), _ptr(q8c.scales),
+        _ptr(k8c.codes), _ptr(k8c.scales), _ptr(v8r.codes), _ptr(v8r.scales), _ptr(o), o_dtype, _ptr(dout),
+        _ptr(lse), B, Hq, Hkv, N, d, float(softmax_scale), int(bool(causal)), _ptr(dq), _ptr(dk), _ptr(dv),
+        _ptr(workspace), workspace.numel(), _stream(dev)))
+    return dq, dk, dv
+
+
+def bf16_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+             softmax_scale: float = 0.0, out_dtype: int = OUT_BF16, with_lse: bool = True, out=None, lse=None):
+    """BF16 FlashAttention forward (fa4bf16_fwd).  Returns (o, lse or None)."""
+    _cuda(q, k, v)
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    if out is None:
+        out = torch.empty((B, Hq, N, d), dtype=torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32, device=q.device)
+    if with_lse and lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    _check("fa4bf16_fwd", load_library().fa4bf16_fwd(
+        _ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, N, d, float(softmax_scale), int(bool(causal)), _ptr(out),
+        out_dtype, _ptr(lse) if with_lse else None, _stream(q.device)))
+    return out, (lse if with_lse else None)
+
+
+def directp_codes(s: torch.Tensor, m: float, c: float) -> torch.Tensor:
+    """Direct-P code of each FP32 score against max m (fa4fp4_directp_codes)."""
+    _cuda(s)
+    if s.dtype != torch.float32:
+        raise ValueError("directp_codes expects float32 scores")
+    out = torch.empty(s.shape, dtype=torch.uint8, device=s.device)
+    _check("fa4fp4_directp_codes", load_library().fa4fp4_directp_codes(
+        _ptr(s), s.numel(), float(m), float(c), _ptr(out), _stream(s.device)))
+    return out
+
+
+def sync_status(device=None):
+    """Synchronize the current stream and raise on a device watchdog error."""
+    _check("fa4fp4_sync_status", load_library().fa4fp4_sync_status(_stream(device)))

@@ -1,0 +1,229 @@
+// api.cu -- the C ABI declared in include/fa4fp4.h: argument validation,
+// TMA tensor-map encoding, the Direct-P threshold constants, kernel launches
+// and the device watchdog word.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include "../../include/fa4fp4.h"
+#include "internal.h"
+
+using namespace fa4;
+
+// Device error word: bounded waits that expire OR a flag in here.
+__device__ unsigned g_fa4fp4_err;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned* g_err_ptr[kMaxDevices] = {};
+
+unsigned* err_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_fa4fp4_err) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned*>(ptr);
+  }
+  return g_err_ptr[dev];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D tiled map over a [d2][d1][d0] tensor of `elem` bytes per element.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem, const void* base, uint64_t d0,
+              uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw) {
+  EncodeTiledFn enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * elem, d0 * d1 * elem};
+  cuuint32_t box[3] = {b0, b1, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Direct-P thresholds: T_k is the smallest FP32 x for which 6*2^x rounds
+// (nearest, ties to even) to at least the k-th E2M1 magnitude.  The rounding
+// switches at the midpoint mu_k below magnitude k; a value exactly on mu_k
+// rounds up only when magnitude k has an even code (1.0, 2.0, 4.0).
+const float* directp_thresholds() {
+  static float T[7];
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const double mu[7] = {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0};
+    for (int k = 1; k <= 7; ++k) {
+      auto reaches = [&](float x) {
+        double v = 6.0 * std::exp2((double)x);
+        return v > mu[k - 1] || (v == mu[k - 1] && (k % 2) == 0);
+      };
+      float x = (float)std::log2(mu[k - 1] / 6.0);
+      while (reaches(std::nextafter(x, -INFINITY))) x = std::nextafter(x, -INFINITY);
+      while (!reaches(x)) x = std::nextafter(x, INFINITY);
+      T[k - 1] = x;
+    }
+  });
+  return T;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+float default_scale(float s, int d) { return s > 0.f ? s : (float)(1.0 / std::sqrt((double)d)); }
+
+fa4fp4_status launch_status(cudaError_t e) { return e == cudaSuccess ? FA4FP4_OK : FA4FP4_ERR_CUDA; }
+
+fa4fp4_status check_dims(int B, int Hq, int Hkv, int N, int d) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || N < 1) return FA4FP4_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA4FP4_ERR_UNSUPPORTED;
+  if (Hkv == 0 ? Hq != 0 : (Hq % Hkv) != 0) return FA4FP4_ERR_UNSUPPORTED;
+  if ((long long)B * Hq * N * d > (1LL << 40)) return FA4FP4_ERR_UNSUPPORTED;
+  return FA4FP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa4fp4_status_string(int s) {
+  switch (s) {
+    case FA4FP4_OK: return "ok";
+    case FA4FP4_ERR_INVALID_ARG: return "invalid argument";
+    case FA4FP4_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case FA4FP4_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case FA4FP4_ERR_CUDA: return "CUDA error";
+    case FA4FP4_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+    case FA4FP4_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+size_t fa4fp4_qtensor_bytes(int B, int H, int N, int d, int fmt, int axis, size_t* scale_bytes) {
+  if (B < 0 || H < 0 || N < 1 || (d != 64 && d != 128) || (fmt != 0 && fmt != 1) ||
+      (axis != 0 && axis != 1)) {
+    if (scale_bytes) *scale_bytes = 0;
+    return 0;
+  }
+  size_t L = axis == 0 ? (size_t)d : (size_t)padded_n(N);
+  size_t R = axis == 0 ? (size_t)N : (size_t)d;
+  size_t per = fmt == 0 ? L / 2 : L;
+  if (scale_bytes) *scale_bytes = (size_t)B * H * R * (L / 32);
+  return (size_t)B * H * R * per;
+}
+
+fa4fp4_status fa4fp4_quantize(const void* x, int B, int H, int N, int d, int fmt, int axis,
+                              void* codes, void* scales, void* stream) {
+  if (!x || !codes || !scales) return FA4FP4_ERR_INVALID_ARG;
+  if ((fmt != 0 && fmt != 1) || (axis != 0 && axis != 1)) return FA4FP4_ERR_INVALID_ARG;
+  fa4fp4_status s = check_dims(B, H, H, N, d);
+  if (s != FA4FP4_OK && !(H == 0 && s == FA4FP4_ERR_UNSUPPORTED)) return s;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return FA4FP4_ERR_ALIGNMENT;
+  if (B == 0 || H == 0) return FA4FP4_OK;
+  long long BH = (long long)B * H;
+  return launch_status(launch_quantize(x, BH * N, d, N, BH, fmt, axis, codes, scales,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+fa4fp4_status fa4fp4_fwd(const void* qc, const void* qs, const void* kc, const void* ks,
+                         const void* vc, const void* vs, int B, int Hq, int Hkv, int N, int d,
+                         float softmax_scale, int causal, void* o, int out_dtype, float* lse,
+                         void* stream) {
+  if (!qc || !qs || !kc || !ks || !vc || !vs || !o) return FA4FP4_ERR_INVALID_ARG;
+  if (out_dtype != FA4FP4_OUT_F32 && out_dtype != FA4FP4_OUT_BF16) return FA4FP4_ERR_INVALID_ARG;
+  fa4fp4_status s = check_dims(B, Hq, Hkv, N, d);
+  if (s != FA4FP4_OK) return s;
+  const void* ptrs[] = {qc, qs, kc, ks, vc, vs, o};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return FA4FP4_ERR_ALIGNMENT;
+  if (lse && !aligned16(lse)) return FA4FP4_ERR_ALIGNMENT;
+  if (B == 0 || Hq == 0) return FA4FP4_OK;
+  FwdFp4Params p;
+  memset(&p, 0, sizeof(p));
+  const int Np = padded_n(N);
+  const CUtensorMapSwizzle qsw = d == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  if (!make_map(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qc, d / 2, N, (uint64_t)B * Hq, d / 2, 128, qsw) ||
+      !make_map(&p.tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kc, d / 2, N, (uint64_t)B * Hkv, d / 2, 128, qsw) ||
+      !make_map(&p.tm_v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, vc, Np / 2, d, (uint64_t)B * Hkv, 64, d,
+                CU_TENSOR_MAP_SWIZZLE_64B))
+    return FA4FP4_ERR_CUDA;
+  p.q_scales = static_cast<const uint8_t*>(qs);
+  p.k_scales = static_cast<const uint8_t*>(ks);
+  p.v_scales = static_cast<const uint8_t*>(vs);
+  p.o = o;
+  p.lse = lse;
+  p.err = err_word();
+  if (!p.err) return FA4FP4_ERR_CUDA;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.Np = Np;
+  p.causal = causal ? 1 : 0;
+  p.out_bf16 = out_dtype == FA4FP4_OUT_BF16;
+  p.scale = default_scale(softmax_scale, d);
+  p.c = (float)((double)p.scale * 1.4426950408889634);
+  const float* T = directp_thresholds();
+  for (int k = 0; k < 7; ++k) p.T[k] = T[k];
+  return launch_status(launch_fwd_fp4(p, static_cast<cudaStream_t>(stream)));
+}
+
+fa4fp4_status fa4fp4_directp_codes(const float* s, int64_t n, float m, float c, uint8_t* codes,
+                                   void* stream) {
+  if (!s || !codes || n < 0) return FA4FP4_ERR_INVALID_ARG;
+  if (n == 0) return FA4FP4_OK;
+  return launch_status(launch_directp_codes(s, n, m, c, directp_thresholds(), codes,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+size_t fa4fp4_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
+  if (check_dims(B, Hq, Hkv, N, d) != FA4FP4_OK) return 0;
+  const size_t rows = (size_t)B * Hq * N;
+  const size_t Np = (size_t)padded_n(N);
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  // dO row view (codes + scales), dO column view (codes + scales), D
+  return up(rows * d) + up(rows * d / 32) + up((size_t)B * Hq * d * Np) +
+         up((size_t)B * Hq * d * Np / 32) + up(rows * sizeof(float));
+}
+
+fa4fp4_status fa4fp4_bwd(const void*, const void*, const void*, const void*, const void*,
+                         const void*, const void*, const void*, const void*, const void*,
+                         const void*, int, const void*, const float*, int, int, int, int, int,
+                         float, int, float*, float*, float*, void*, size_t, void*) {
+  return FA4FP4_ERR_UNSUPPORTED;
+}
+
+fa4fp4_status fa4bf16_fwd(const void*, const void*, const void*, int, int, int, int, int, float,
+                          int, void*, int, float*, void*) {
+  return FA4FP4_ERR_UNSUPPORTED;
+}
+
+fa4fp4_status fa4fp4_sync_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return FA4FP4_ERR_CUDA;
+  unsigned* w = err_word();
+  if (!w) return FA4FP4_ERR_CUDA;
+  unsigned host = 0;
+  if (cudaMemcpy(&host, w, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) return FA4FP4_ERR_CUDA;
+  if (host) {
+    unsigned zero = 0;
+    cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    return FA4FP4_ERR_DEVICE_TIMEOUT;
+  }
+  return FA4FP4_OK;
+}
+
+}  // extern "C"

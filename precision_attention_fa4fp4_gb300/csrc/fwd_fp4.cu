@@ -1,0 +1,406 @@
+// fwd_fp4.cu -- Direct-P FP4 attention forward for sm_103a.
+//
+// "Hardware-Aware FP4 FlashAttention-4" (arXiv:2609.04105), technical
+// summary, Methodology 1: S = Q K^T on FP4 tensor cores; each score's offset
+// from the running row max classified straight into an E2M1 probability code
+// ("Direct Mapping"); the normalizer accumulated from the same codes the P V
+// product consumes ("Consistent Normalization"); MXFP4 for P and V ("Format
+// Selection").  Q and K are MXFP4 as well.
+//
+// One CTA per (batch*head, 128-query tile), 6 warps:
+//   warp 0     producer: TMA loads of Q, K_j, V^T_j codes into swizzled shared
+//              memory; their E8M0 scales rearranged into the 32x16-byte chunks
+//              the scale-factor TMEM copy expects.
+//   warp 1     TMEM allocation; one elected lane issues tcgen05.cp for scale
+//              factors and tcgen05.mma (kind::mxf4, block_scale) for
+//              S_j = Q K_j^T into a double-buffered S and O += P_j V_j.
+//   warps 2-5  softmax: one query row per thread (TMEM lane quadrant =
+//              warp % 4).  Row max, Direct-P codes, code-sum normalizer, the
+//              eager O rescale in TMEM, packed P codes to shared memory.
+// The QK^T of tile j+1 runs on the tensor core while tile j's codes are built.
+#include <cuda_bf16.h>
+#include "common.cuh"
+#include "internal.h"
+
+namespace fa4 {
+namespace {
+
+constexpr int BM = 128;         // queries per CTA
+constexpr int BN = 128;         // keys per tile
+constexpr int STAGES = 6;       // K/V pipeline depth
+constexpr int NTHREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_SFQ = 384, COL_SFP = 388,
+                   COL_SFK = 392, COL_SFV = 392 + 4 * STAGES;
+
+template <int D>
+struct Smem {
+  static constexpr int QB = BM * D / 2;   // bytes of a Q or K code tile
+  static constexpr int KB = BN * D / 2;
+  static constexpr int VB = D * BN / 2;   // V^T: D rows of 128 keys
+  static constexpr int PB = BM * BN / 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + QB;
+  static constexpr int OFF_V = OFF_K + STAGES * KB;
+  static constexpr int OFF_P = OFF_V + STAGES * VB;
+  static constexpr int OFF_SF = OFF_P + 2 * PB;           // 512-byte scale chunks
+  static constexpr int SF_Q = OFF_SF, SF_P = SF_Q + 512, SF_K = SF_P + 512,
+                       SF_V = SF_K + 512 * STAGES;
+  static constexpr int OFF_BAR = SF_V + 512 * STAGES;
+  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 1 + 1 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
+  static constexpr int BYTES = OFF_MISC + 64 + 1024;    // + alignment slack
+};
+
+// Direct-P code of one scaled offset x: #{k : x >= T_k}.
+FA4_DEV uint32_t directp_code(float x, const float (&T)[7]) {
+  uint32_t c = 0;
+#pragma unroll
+  for (int k = 0; k < 7; ++k) c += (x >= T[k]) ? 1u : 0u;
+  return c;
+}
+
+// Sum of E2M1 magnitudes (times 2) of the 8 codes packed in w.
+FA4_DEV uint32_t code_sum2(uint32_t w, uint32_t acc) {
+  const uint32_t lo = 0x03020100u, hi = 0x0C080604u;   // 2*{0,.5,1,1.5,2,3,4,6}
+  acc = __dp4a(__byte_perm(lo, hi, w & 0xffffu), 0x01010101u, acc);
+  acc = __dp4a(__byte_perm(lo, hi, w >> 16), 0x01010101u, acc);
+  return acc;
+}
+
+// Rearrange 128 rows of per-row scale words into the scale-factor chunk:
+// chunk byte (r%32)*16 + (r/32)*4 + kblock.  Called by a full warp.
+FA4_DEV void stage_sf_rows(uint8_t* chunk, const uint8_t* src, int row0, int nrows_valid,
+                           int bytes_per_row, int lane) {
+  uint32_t w[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    int r = lane + 32 * c;
+    uint32_t v = 0;
+    if (r < nrows_valid) {
+      const uint8_t* p = src + (long long)(row0 + r) * bytes_per_row;
+      v = bytes_per_row == 4 ? *reinterpret_cast<const uint32_t*>(p)
+                             : (uint32_t)*reinterpret_cast<const uint16_t*>(p);
+    }
+    w[c] = v;
+  }
+  *reinterpret_cast<uint4*>(chunk + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_constant__ FwdFp4Params p) {
+  using L = Smem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + STAGES;
+  uint64_t* s_full = kv_empty + STAGES;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_free + 2;
+  uint64_t* o_done = p_full + 1;
+  uint64_t* mma_done = o_done + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int nq = (p.N + BM - 1) / BM;
+  const int qt = p.causal ? (nq - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+  const int bh = blockIdx.y;
+  const int b = bh / p.Hq, h = bh % p.Hq;
+  const int bkv = b * p.Hkv + h / (p.Hq / p.Hkv);
+  const int q0 = qt * BM;
+  const int nk_all = (p.N + BN - 1) / BN;
+  const int nt = p.causal ? min(nk_all, qt + 1) : nk_all;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < STAGES; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
+    for (int s = 0; s < 2; ++s) { mbar_init(&s_full[s], 1); mbar_init(&s_free[s], 4); }
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    // unit E8M0 scale (byte 127) for every P block
+    reinterpret_cast<uint4*>(smem + L::SF_P)[lane] = make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
+    fence_proxy_async_smem();
+    tmem_alloc(tmem_holder, TMEM_COLS);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+    }
+    stage_sf_rows(smem + L::SF_Q, p.q_scales + (long long)bh * p.N * (D / 32), q0,
+                  min(BM, p.N - q0), D / 32, lane);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, L::QB);
+      tma_load_3d(smem + L::OFF_Q, &p.tm_q, q_full, 0, q0, bh);
+    }
+    const uint8_t* ks = p.k_scales + (long long)bkv * p.N * (D / 32);
+    const uint8_t* vs = p.v_scales + (long long)bkv * D * (p.Np / 32);
+    int issued = 0;
+    for (int j = 0; j < nt; ++j) {
+      const int st = j % STAGES;
+      if (j >= STAGES && !mbar_wait(&kv_empty[st], ((j / STAGES) - 1) & 1, abort_flag, p.err)) break;
+      stage_sf_rows(smem + L::SF_K + 512 * st, ks, j * BN, min(BN, p.N - j * BN), D / 32, lane);
+      // V^T scales: channel rows, 4 key blocks of tile j
+      {
+        uint32_t w[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          int ch = lane + 32 * c;
+          w[c] = ch < D ? *reinterpret_cast<const uint32_t*>(vs + (long long)ch * (p.Np / 32) + 4 * j) : 0u;
+        }
+        *reinterpret_cast<uint4*>(smem + L::SF_V + 512 * st + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&kv_full[st], L::KB + L::VB);
+        tma_load_3d(smem + L::OFF_K + st * L::KB, &p.tm_k, &kv_full[st], 0, j * BN, bkv);
+        tma_load_3d(smem + L::OFF_V + st * L::VB, &p.tm_v, &kv_full[st], j * (BN / 2), 0, bkv);
+      }
+      issued = j + 1;
+    }
+    // drain: never leave a bulk copy in flight into this CTA's shared memory
+    if (*abort_flag && lane == 0) {
+      volatile int no_abort = 0;
+      for (int j = max(0, issued - STAGES); j < issued; ++j)
+        mbar_wait(&kv_full[j % STAGES], (j / STAGES) & 1, &no_abort, p.err);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr int KSTEPS = D / 64;   // K = 64 per mxf4 MMA
+      const uint32_t idesc_s = idesc_bs(BM, BN, 1, 1, false, false, 0, 0);
+      const uint32_t idesc_o = idesc_bs(BM, D, 1, 1, false, false, 0, 0);
+      constexpr Swizzle QSW = D == 128 ? SW_64B : SW_32B;
+      constexpr uint32_t QSBO = D == 128 ? 512 : 256;
+      const uint32_t sq = smem_u32(smem + L::OFF_Q);
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
+      tc_fence_after();
+      if (ok) {
+        tmem_cp_sf(tbase + COL_SFQ, smem + L::SF_Q);
+        tmem_cp_sf(tbase + COL_SFP, smem + L::SF_P);
+      }
+      auto issue_pv = [&](int t) -> bool {
+        if (!mbar_wait(p_full, t & 1, abort_flag, p.err)) return false;
+        tc_fence_after();
+        const int st = t % STAGES;
+        const uint32_t sp = smem_u32(smem + L::OFF_P + (t & 1) * L::PB);
+        const uint32_t sv = smem_u32(smem + L::OFF_V + st * L::VB);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {     // 128 keys = 2 x K64
+          uint64_t ad = make_sdesc(sp + 32 * k, 16, 512, SW_64B);
+          uint64_t bd = make_sdesc(sv + 32 * k, 16, 512, SW_64B);
+          uint32_t id = idesc_o | ((uint32_t)(2 * k) << 29) | ((uint32_t)(2 * k) << 4);
+          mma_mxf4(tbase + COL_O, ad, bd, id, tbase + COL_SFP, tbase + COL_SFV + 4 * st, t > 0 || k > 0);
+        }
+        mma_commit(o_done);
+        mma_commit(&kv_empty[st]);
+        return true;
+      };
+      for (int j = 0; ok && j < nt; ++j) {
+        const int st = j % STAGES;
+        if (!mbar_wait(&kv_full[st], (j / STAGES) & 1, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        tmem_cp_sf(tbase + COL_SFK + 4 * st, smem + L::SF_K + 512 * st);
+        tmem_cp_sf(tbase + COL_SFV + 4 * st, smem + L::SF_V + 512 * st);
+        const int sb = j & 1;
+        if (j >= 2 && !mbar_wait(&s_free[sb], ((j >> 1) - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sk = smem_u32(smem + L::OFF_K + st * L::KB);
+#pragma unroll
+        for (int k = 0; k < KSTEPS; ++k) {
+          uint64_t ad = make_sdesc(sq + 32 * k, 16, QSBO, QSW);
+          uint64_t bd = make_sdesc(sk + 32 * k, 16, QSBO, QSW);
+          uint32_t id = idesc_s | ((uint32_t)(2 * k) << 29) | ((uint32_t)(2 * k) << 4);
+          mma_mxf4(tbase + (sb ? COL_S1 : COL_S0), ad, bd, id, tbase + COL_SFQ, tbase + COL_SFK + 4 * st, k > 0);
+        }
+        mma_commit(&s_full[sb]);
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok && nt > 0) issue_pv(nt - 1);
+      // all tcgen05 work of this thread completes before TMEM is released
+      mma_commit(mma_done);
+      volatile int no_abort = 0;
+      mbar_wait(mma_done, 0, &no_abort, p.err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int qi = q0 + r;
+    const uint32_t lane_base = tbase + ((uint32_t)(quad * 32) << 16);
+    const float c = p.c;
+    float T[7];
+#pragma unroll
+    for (int k = 0; k < 7; ++k) T[k] = p.T[k];
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    uint8_t* prow_base = smem + L::OFF_P + r * 64;
+    for (int j = 0; j < nt; ++j) {
+      const int sb = j & 1;
+      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
+      tc_fence_after();
+      float s[BN];
+#pragma unroll
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + (sb ? COL_S1 : COL_S0) + cc * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(v[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
+      const int kbase = j * BN;
+      if (kbase + BN > p.N || (p.causal && kbase + BN - 1 > q0)) {
+        const int lim = p.causal ? min(p.N - 1, qi) : p.N - 1;
+#pragma unroll
+        for (int i = 0; i < BN; ++i)
+          if (kbase + i > lim) s[i] = -INFINITY;
+      }
+      float tmax = s[0];
+#pragma unroll
+      for (int i = 1; i + 1 < BN; i += 2) tmax = fmax3(tmax, s[i], s[i + 1]);
+      tmax = fmaxf(tmax, s[BN - 1]);
+      const float m_new = fmaxf(m, tmax);
+      const float mc = m_new * c;
+      uint32_t pw[BN / 8];
+      uint32_t acc = 0;
+#pragma unroll
+      for (int w = 0; w < BN / 8; ++w) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) word |= directp_code(fmaf(s[w * 8 + e], c, -mc), T) << (4 * e);
+        pw[w] = word;
+        acc = code_sum2(word, acc);
+      }
+      const float alpha = (m == -INFINITY) ? 1.f : ex2_approx(fmaf(m, c, -mc));
+      if (j > 0) {
+        if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t v[32];
+            tmem_ld32(lane_base + COL_O + cc * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(lane_base + COL_O + cc * 32, v);
+          }
+          tmem_st_wait();
+        }
+      }
+      l = alpha * l + 0.5f * (float)acc;
+      m = m_new;
+      // packed codes of this row -> P[j&1], 64-byte row, 64B swizzle
+      uint8_t* prow = prow_base + sb * L::PB;
+      const int x = (r >> 1) & 3;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<uint4*>(prow + ((k ^ x) << 4)) =
+            make_uint4(pw[4 * k], pw[4 * k + 1], pw[4 * k + 2], pw[4 * k + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (ok && nt > 0 && mbar_wait(o_done, (nt - 1) & 1, abort_flag, p.err)) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const bool valid = qi < p.N;
+      const long long orow = ((long long)bh * p.N + qi) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + COL_O + cc * 32, v);
+        tmem_ld_wait();
+        if (valid) {
+          if (p.out_bf16) {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow + cc * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(v[q * 8 + 2 * e]) * inv_l,
+                                                         __uint_as_float(v[q * 8 + 2 * e + 1]) * inv_l);
+                w[e] = *reinterpret_cast<uint32_t*>(&t);
+              }
+              dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + orow + cc * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv_l, __uint_as_float(v[4 * q + 1]) * inv_l,
+                                   __uint_as_float(v[4 * q + 2]) * inv_l, __uint_as_float(v[4 * q + 3]) * inv_l);
+          }
+        }
+      }
+      if (valid && p.lse) p.lse[(long long)bh * p.N + qi] = p.scale * m + logf(l * (1.f / 6.f));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tbase, TMEM_COLS);
+}
+
+__global__ void directp_codes_kernel(const float* __restrict__ s, long long n, float m, float c,
+                                     Thresh T, uint8_t* __restrict__ out) {
+  float t[7];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) t[k] = T.v[k];
+  const float mc = m * c;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    out[i] = (uint8_t)directp_code(fmaf(s[i], c, -mc), t);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_fp4(const FwdFp4Params& p, cudaStream_t st) {
+  const int nq = (p.N + BM - 1) / BM;
+  dim3 grid(nq, p.B * p.Hq);
+  if (p.d == 128) {
+    auto k = fwd_fp4_kernel<128>;
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<128>::BYTES);
+    k<<<grid, NTHREADS, Smem<128>::BYTES, st>>>(p);
+  } else {
+    auto k = fwd_fp4_kernel<64>;
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<64>::BYTES);
+    k<<<grid, NTHREADS, Smem<64>::BYTES, st>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_directp_codes(const float* s, long long n, float m, float c, const float* T,
+                                 uint8_t* codes, cudaStream_t st) {
+  Thresh t;
+  for (int k = 0; k < 7; ++k) t.v[k] = T[k];
+  long long blocks = (n + 255) / 256;
+  int grid = (int)(blocks < 152 * 16 ? (blocks > 0 ? blocks : 1) : 152 * 16);
+  directp_codes_kernel<<<grid, 256, 0, st>>>(s, n, m, c, t, codes);
+  return cudaGetLastError();
+}
+
+}  // namespace fa4

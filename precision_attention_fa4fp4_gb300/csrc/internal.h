@@ -1,0 +1,74 @@
+// internal.h -- host-side declarations shared by the library's translation
+// units (kernel launchers and their parameter blocks).  Not part of the ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa4 {
+
+struct Thresh { float v[7]; };
+
+// Round N up to the padded key length of the along-N layouts.
+inline int padded_n(int N) { return (N + 127) / 128 * 128; }
+
+// ---------------------------------------------------------------- quantize
+cudaError_t launch_quantize(const void* x, long long rows, int d, int N, long long BH, int fmt,
+                            int axis, void* codes, void* scales, cudaStream_t st);
+
+// ---------------------------------------------------------------- FP4 fwd
+struct FwdFp4Params {
+  CUtensorMap tm_q, tm_k, tm_v;     // MXFP4 codes of Q, K (along d) and V^T (along N)
+  const uint8_t* q_scales;
+  const uint8_t* k_scales;
+  const uint8_t* v_scales;
+  void* o;
+  float* lse;
+  unsigned* err;
+  int B, Hq, Hkv, N, d, Np, causal, out_bf16;
+  float scale, c;                   // softmax scale, fl32(scale*log2 e)
+  float T[7];                       // Direct-P thresholds
+};
+cudaError_t launch_fwd_fp4(const FwdFp4Params& p, cudaStream_t st);
+cudaError_t launch_directp_codes(const float* s, long long n, float m, float c, const float* T,
+                                 uint8_t* codes, cudaStream_t st);
+
+// ---------------------------------------------------------------- BF16 fwd
+struct FwdBf16Params {
+  CUtensorMap tm_q, tm_k, tm_v;     // bf16 Q, K, V
+  void* o;
+  float* lse;
+  unsigned* err;
+  int B, Hq, Hkv, N, d, causal, out_bf16;
+  float scale, c;
+};
+cudaError_t launch_fwd_bf16(const FwdBf16Params& p, cudaStream_t st);
+
+// ---------------------------------------------------------------- bwd
+struct BwdParams {
+  CUtensorMap tm_q4, tm_k4;          // MXFP4 codes (along d)
+  CUtensorMap tm_q8c, tm_k8c;        // MXFP8 column views [bh][d][Np]
+  CUtensorMap tm_v8r;                // MXFP8 row view of V [bh][N][d]
+  CUtensorMap tm_do_r, tm_do_c;      // MXFP8 views of dO (workspace)
+  const uint8_t *q4_s, *k4_s, *q8c_s, *k8c_s, *v8r_s, *do_r_s, *do_c_s;
+  const float* lse;
+  const float* Dvec;                 // rowsum(dO*O), workspace
+  float *dq, *dk, *dv;
+  unsigned* err;
+  int B, Hq, Hkv, N, d, Np, causal;
+  float scale, c, l2e;
+};
+struct BwdPrepParams {
+  const void* o;
+  const void* dout;
+  int o_bf16;
+  int B, Hq, N, d, Np;
+  uint8_t *do_r, *do_r_s, *do_c, *do_c_s;
+  float* Dvec;
+  float* dq;
+};
+cudaError_t launch_bwd_prep(const BwdPrepParams& p, cudaStream_t st);
+cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t st);
+
+}  // namespace fa4

@@ -1,0 +1,183 @@
+// quantize.cu -- MXFP4 / MXFP8 block quantization (OCP MX rule).
+//
+// "Hardware-Aware FP4 FlashAttention-4", technical summary, Methodology 1
+// ("Format Selection": power-of-two block scales over 32-element fragments)
+// and Methodology 2 ("Gradient Formats": row/column-oriented FP8 views).
+//
+// Per block of 32 values: amax, E8M0 exponent X = E(amax) - 127 - emax
+// (emax = 2 for E2M1, 8 for E4M3; clamped to [-127,127]), elements x*2^-X
+// converted with round-to-nearest-even and saturation by the hardware
+// converters.  The kernels are HBM-bound: 16-byte coalesced loads, one thread
+// per block for blocks along d, and a shared-memory transpose of 128-token
+// tiles for blocks along N.
+#include <cuda_bf16.h>
+#include "common.cuh"
+#include "internal.h"
+
+namespace fa4 {
+namespace {
+
+FA4_DEV float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+FA4_DEV float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// exponent of the block: returns X, writes 2^-X to *inv
+template <int FMT>
+FA4_DEV int block_exp(float amax, float* inv) {
+  constexpr int emax = FMT == 0 ? 2 : 8;
+  int E = (int)((__float_as_uint(amax) >> 23) & 0xff);
+  int X = E - 127 - emax;
+  X = X < -127 ? -127 : (X > 127 ? 127 : X);
+  *inv = __uint_as_float((uint32_t)(127 - X) << 23);
+  return X;
+}
+
+// blocks along d: one thread per 32-element block.
+template <int FMT>
+__global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict__ x,
+                                                          long long nblocks,
+                                                          uint8_t* __restrict__ codes,
+                                                          uint8_t* __restrict__ scales) {
+  for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nblocks;
+       b += (long long)gridDim.x * blockDim.x) {
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __ldg(x + b * 4 + i);
+    float f[32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        f[i * 8 + 2 * j] = bf_lo(w[j]);
+        f[i * 8 + 2 * j + 1] = bf_hi(w[j]);
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    float inv;
+    int X = block_exp<FMT>(amax, &inv);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] *= inv;
+    scales[b] = (uint8_t)(X + 127);
+    if (FMT == 0) {
+      uint4 o;
+      o.x = pack_e2m1x8(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]);
+      o.y = pack_e2m1x8(f[8], f[9], f[10], f[11], f[12], f[13], f[14], f[15]);
+      o.z = pack_e2m1x8(f[16], f[17], f[18], f[19], f[20], f[21], f[22], f[23]);
+      o.w = pack_e2m1x8(f[24], f[25], f[26], f[27], f[28], f[29], f[30], f[31]);
+      reinterpret_cast<uint4*>(codes)[b] = o;
+    } else {
+      uint4 o0, o1;
+      o0.x = pack_e4m3x4(f[0], f[1], f[2], f[3]);
+      o0.y = pack_e4m3x4(f[4], f[5], f[6], f[7]);
+      o0.z = pack_e4m3x4(f[8], f[9], f[10], f[11]);
+      o0.w = pack_e4m3x4(f[12], f[13], f[14], f[15]);
+      o1.x = pack_e4m3x4(f[16], f[17], f[18], f[19]);
+      o1.y = pack_e4m3x4(f[20], f[21], f[22], f[23]);
+      o1.z = pack_e4m3x4(f[24], f[25], f[26], f[27]);
+      o1.w = pack_e4m3x4(f[28], f[29], f[30], f[31]);
+      reinterpret_cast<uint4*>(codes)[2 * b] = o0;
+      reinterpret_cast<uint4*>(codes)[2 * b + 1] = o1;
+    }
+  }
+}
+
+// blocks along N: CTA = one (b,h) x 128-token tile, output transposed
+// [bh][d][Np].  Shared tile [128 tokens][d] bf16; thread (channel, 32-token
+// block) with consecutive threads on consecutive channels.
+template <int FMT, int D>
+__global__ void __launch_bounds__(256) quant_cols_kernel(const __nv_bfloat16* __restrict__ x,
+                                                          int N, int Np,
+                                                          uint8_t* __restrict__ codes,
+                                                          uint8_t* __restrict__ scales) {
+  __shared__ __align__(16) __nv_bfloat16 tile[128 * D];
+  const int t0 = blockIdx.x * 128;
+  const long long bh = blockIdx.y;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (bh * N + t0) * (long long)D);
+  const int valid = min(128, N - t0);
+  constexpr int VEC = D / 8;   // uint4 per token row
+  for (int i = threadIdx.x; i < 128 * VEC; i += blockDim.x) {
+    int tok = i / VEC;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (tok < valid) v = __ldg(src + i);
+    reinterpret_cast<uint4*>(tile)[i] = v;
+  }
+  __syncthreads();
+  constexpr int BYTES = FMT == 0 ? 16 : 32;    // code bytes per 32-token block
+  for (int u = threadIdx.x; u < D * 4; u += blockDim.x) {
+    const int ch = u % D, kb = u / D;
+    float f[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] = __bfloat162float(tile[(kb * 32 + i) * D + ch]);
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    float inv;
+    int X = block_exp<FMT>(amax, &inv);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] *= inv;
+    const long long row = bh * D + ch;
+    scales[row * (Np / 32) + t0 / 32 + kb] = (uint8_t)(X + 127);
+    uint8_t* dst = codes + row * (long long)(Np * BYTES / 32) + (t0 / 32 + kb) * BYTES;
+    if (FMT == 0) {
+      uint4 o;
+      o.x = pack_e2m1x8(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]);
+      o.y = pack_e2m1x8(f[8], f[9], f[10], f[11], f[12], f[13], f[14], f[15]);
+      o.z = pack_e2m1x8(f[16], f[17], f[18], f[19], f[20], f[21], f[22], f[23]);
+      o.w = pack_e2m1x8(f[24], f[25], f[26], f[27], f[28], f[29], f[30], f[31]);
+      *reinterpret_cast<uint4*>(dst) = o;
+    } else {
+      uint4 o0, o1;
+      o0.x = pack_e4m3x4(f[0], f[1], f[2], f[3]);
+      o0.y = pack_e4m3x4(f[4], f[5], f[6], f[7]);
+      o0.z = pack_e4m3x4(f[8], f[9], f[10], f[11]);
+      o0.w = pack_e4m3x4(f[12], f[13], f[14], f[15]);
+      o1.x = pack_e4m3x4(f[16], f[17], f[18], f[19]);
+      o1.y = pack_e4m3x4(f[20], f[21], f[22], f[23]);
+      o1.z = pack_e4m3x4(f[24], f[25], f[26], f[27]);
+      o1.w = pack_e4m3x4(f[28], f[29], f[30], f[31]);
+      reinterpret_cast<uint4*>(dst)[0] = o0;
+      reinterpret_cast<uint4*>(dst)[1] = o1;
+    }
+  }
+}
+
+int grid_for(long long work, int per_cta) {
+  int sms = 152;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long need = (work + per_cta - 1) / per_cta;
+  long long cap = (long long)sms * 8;
+  return (int)(need < cap ? (need > 0 ? need : 1) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const void* x, long long rows, int d, int N, long long BH, int fmt,
+                            int axis, void* codes, void* scales, cudaStream_t st) {
+  if (axis == 0) {
+    long long nblocks = rows * (d / 32);
+    int grid = grid_for(nblocks, 256);
+    if (fmt == 0)
+      quant_rows_kernel<0><<<grid, 256, 0, st>>>((const uint4*)x, nblocks, (uint8_t*)codes,
+                                                 (uint8_t*)scales);
+    else
+      quant_rows_kernel<1><<<grid, 256, 0, st>>>((const uint4*)x, nblocks, (uint8_t*)codes,
+                                                 (uint8_t*)scales);
+  } else {
+    int Np = padded_n(N);
+    dim3 grid(Np / 128, (unsigned)BH);
+    const __nv_bfloat16* xb = (const __nv_bfloat16*)x;
+    if (d == 128) {
+      if (fmt == 0) quant_cols_kernel<0, 128><<<grid, 256, 0, st>>>(xb, N, Np, (uint8_t*)codes, (uint8_t*)scales);
+      else quant_cols_kernel<1, 128><<<grid, 256, 0, st>>>(xb, N, Np, (uint8_t*)codes, (uint8_t*)scales);
+    } else {
+      if (fmt == 0) quant_cols_kernel<0, 64><<<grid, 256, 0, st>>>(xb, N, Np, (uint8_t*)codes, (uint8_t*)scales);
+      else quant_cols_kernel<1, 64><<<grid, 256, 0, st>>>(xb, N, Np, (uint8_t*)codes, (uint8_t*)scales);
+    }
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fa4

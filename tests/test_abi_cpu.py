@@ -1,0 +1,72 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point include/fa4fp4.h declares, sizes its buffers, and rejects bad
+arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from precision_attention_fa4fp4_gb300 import api, build
+    build.build()
+    return api.load_library()
+
+
+def declared_symbols():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            txt = open(os.path.join(inc, f)).read()
+            names |= set(re.findall(r"FA4FP4_API\s+[\w\s\*]+?\b(\w+)\s*\(", txt))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_qtensor_bytes(lib):
+    sb = ctypes.c_size_t(0)
+    assert lib.fa4fp4_qtensor_bytes(2, 3, 300, 128, 0, 0, ctypes.byref(sb)) == 2 * 3 * 300 * 64
+    assert sb.value == 2 * 3 * 300 * 4
+    assert lib.fa4fp4_qtensor_bytes(2, 3, 300, 128, 0, 1, ctypes.byref(sb)) == 2 * 3 * 128 * 384 // 2
+    assert sb.value == 2 * 3 * 128 * 384 // 32
+    assert lib.fa4fp4_qtensor_bytes(1, 1, 33, 64, 1, 1, ctypes.byref(sb)) == 64 * 128
+    assert lib.fa4fp4_qtensor_bytes(1, 1, 33, 96, 0, 0, ctypes.byref(sb)) == 0
+    assert lib.fa4fp4_qtensor_bytes(1, 1, 0, 64, 0, 0, None) == 0
+
+
+def test_argument_errors_before_launch(lib):
+    p = ctypes.c_void_p(4096)       # never dereferenced: validation fails first
+    odd = ctypes.c_void_p(4097)
+    null = None
+    INVALID, UNSUP, ALIGN = 1, 2, 3
+    assert lib.fa4fp4_quantize(null, 1, 1, 32, 64, 0, 0, p, p, null) == INVALID
+    assert lib.fa4fp4_quantize(p, 1, 1, 32, 64, 2, 0, p, p, null) == INVALID
+    assert lib.fa4fp4_quantize(p, 1, 1, 32, 96, 0, 0, p, p, null) == UNSUP
+    assert lib.fa4fp4_quantize(odd, 1, 1, 32, 64, 0, 0, p, p, null) == ALIGN
+    args = [p] * 6
+    assert lib.fa4fp4_fwd(*args, 1, 4, 3, 64, 64, 0.0, 0, p, 1, null, null) == UNSUP   # Hq % Hkv
+    assert lib.fa4fp4_fwd(*args, 1, 4, 4, 64, 80, 0.0, 0, p, 1, null, null) == UNSUP   # d
+    assert lib.fa4fp4_fwd(*args, 1, 4, 4, 0, 64, 0.0, 0, p, 1, null, null) == INVALID  # N
+    assert lib.fa4fp4_fwd(*args, 1, 4, 4, 64, 64, 0.0, 0, p, 7, null, null) == INVALID # dtype
+    assert lib.fa4fp4_fwd(*([p] * 5 + [odd]), 1, 4, 4, 64, 64, 0.0, 0, p, 1, null, null) == ALIGN
+    assert lib.fa4bf16_fwd(null, p, p, 1, 1, 1, 64, 64, 0.0, 0, p, 1, null, null) == INVALID
+    assert lib.fa4fp4_directp_codes(null, 10, 0.0, 1.0, p, null) == INVALID
+    assert lib.fa4fp4_status_string(5).decode() == "device pipeline wait timed out"
+
+
+def test_workspace_size(lib):
+    n = lib.fa4fp4_bwd_workspace_bytes(2, 4, 2, 300, 128)
+    rows = 2 * 4 * 300
+    assert n >= rows * 128 + rows * 4 + 2 * 4 * 128 * 384 + rows * 4
+    assert lib.fa4fp4_bwd_workspace_bytes(2, 4, 3, 300, 128) == 0

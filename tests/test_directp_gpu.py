@@ -1,0 +1,37 @@
+"""The device Direct-P classifier vs the oracle's map, bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def test_every_fp32_offset_in_range():
+    """All FP32 x in [-6, 0.5] with |x| >= 2^-8 (every threshold lies in
+    [-4.59, -0.26]; smaller |x| are code 7), plus specials (m=0, c=1 makes
+    x = s exactly)."""
+    fa = require_gpu()
+    lo = np.float32(-6.0)
+    neg = np.arange(np.float32(2.0 ** -8).view(np.int32), lo.view(np.int32) + 1, dtype=np.int32)
+    pos = np.arange(np.float32(2.0 ** -8).view(np.int32), np.float32(0.5).view(np.int32) + 1, dtype=np.int32)
+    x = np.concatenate([-(neg.view(np.float32)), pos.view(np.float32),
+                        np.array([0.0, -0.0, -np.inf, -100.0, 1e-30, -1e-30], np.float32)])
+    got = fa.directp_codes(torch.from_numpy(x).cuda(), 0.0, 1.0).cpu().numpy()
+    want = oracle.directp_codes_of_x(x)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, f"{bad.size} codes differ, e.g. x={x[bad[:5]]} gpu={got[bad[:5]]} oracle={want[bad[:5]]}"
+
+
+def test_random_scores_and_maxima():
+    fa = require_gpu()
+    rng = np.random.default_rng(0)
+    for _ in range(20):
+        m = np.float32(rng.standard_normal() * 30)
+        c = np.float32(rng.uniform(0.05, 0.3))
+        s = (m - np.abs(rng.standard_normal(100000)) * 40).astype(np.float32)
+        got = fa.directp_codes(torch.from_numpy(s).cuda(), float(m), float(c)).cpu().numpy()
+        want = np.array([oracle.directp_code(float(v), float(m), float(c)) for v in s[:3000]])
+        assert np.array_equal(got[:3000], want)
