@@ -1,0 +1,402 @@
+"""Benchmark: FP4 Direct-P attention forward TFLOP/s (noncausal, d=128) and its
+speedup over the library's own BF16 FlashAttention forward, on one GB300.
+
+Workload (one step): bf16 Q, K, V of shape [4,16,4096,128] resident in HBM ->
+fa4fp4_quantize Q, K (MXFP4 along d) and V (MXFP4 along N) -> fa4fp4_fwd
+(Direct-P, noncausal) -> O bf16 + LSE.  FLOPs per step: 4*B*H*N^2*d.
+L2 is flushed (a 256 MiB write) before every timed step; each step is timed
+with CUDA events on the launching stream.
+
+Also reported: the forward kernel alone (the roofline line), the BF16 kernel on
+the same inputs, the causal GQA training config (forward + backward) and an
+end-to-end figure through host buffers.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun every rank runs its own copy of the workload (independent
+problems, no data-path collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from precision_attention_fa4fp4_gb300.inputs import FWD_4K, TRAIN_8B, make_inputs  # noqa: E402
+
+METRIC = "FP4 attention fwd TFLOP/s (noncausal, d=128) and speedup vs own BF16 kernel"
+FP4_OVER_BF16 = 13.5 / 2.25     # nominal dense FP4 : BF16 tensor rate on GB300
+FP8_OVER_BF16 = 4.5 / 2.25
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            mp = json.load(f)
+        return {"bf16": float(mp["bf16_tflops"]), "bf16_sustained": float(mp["bf16_tflops_sustained"]),
+                "hbm": float(mp["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (barrier + max over ranks only)
+# ----------------------------------------------------------------------------
+def dist_setup(ngpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        load = [s for s in sm if s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# the timed loops
+# ----------------------------------------------------------------------------
+class Flusher:
+    def __init__(self, dev):
+        self.buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        self.buf.zero_()
+
+
+def time_steps(step, warmup, steps, flush, world, inner=None):
+    """Returns (per-step ms list, per-step inner-kernel ms list or None)."""
+    for _ in range(warmup):
+        flush()
+        step(None)
+    barrier(world)
+    outer, inner_ms = [], []
+    evs = []
+    for _ in range(steps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ie = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] if inner else None
+        e0.record()
+        step(ie)
+        e1.record()
+        evs.append((e0, e1, ie))
+    barrier(world)
+    for e0, e1, ie in evs:
+        outer.append(e0.elapsed_time(e1))
+        if ie:
+            inner_ms.append(ie[0].elapsed_time(ie[1]))
+    return outer, (inner_ms if inner else None)
+
+
+def run_ours(args, rank, world, local):
+    import precision_attention_fa4fp4_gb300 as fa
+    fa.load_library()
+    dev = torch.device("cuda", local)
+    w = FWD_4K
+    q, k, v = (t.to(dev) for t in make_inputs(w, seed=rank))
+    B, H, N, d = w.B, w.Hq, w.N, w.d
+    q4 = fa.qtensor_alloc(B, H, N, d, fa.FMT_MXFP4, fa.ALONG_D, dev)
+    k4 = fa.qtensor_alloc(B, H, N, d, fa.FMT_MXFP4, fa.ALONG_D, dev)
+    vt = fa.qtensor_alloc(B, H, N, d, fa.FMT_MXFP4, fa.ALONG_N, dev)
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    flush = Flusher(dev)
+
+    def step(ie):
+        fa.quantize(q, fa.FMT_MXFP4, fa.ALONG_D, out=q4)
+        fa.quantize(k, fa.FMT_MXFP4, fa.ALONG_D, out=k4)
+        fa.quantize(v, fa.FMT_MXFP4, fa.ALONG_N, out=vt)
+        if ie:
+            ie[0].record()
+        fa.fwd(q4, k4, vt, causal=False, out_dtype=fa.OUT_BF16, out=o, lse=lse)
+        if ie:
+            ie[1].record()
+
+    def step_bf16(ie):
+        fa.bf16_fwd(q, k, v, causal=False, out_dtype=fa.OUT_BF16, out=o, lse=lse)
+
+    def step_fwd_only(ie):
+        fa.fwd(q4, k4, vt, causal=False, out_dtype=fa.OUT_BF16, out=o, lse=lse)
+
+    clocks = ClockSampler(local) if rank == 0 else None
+    t0 = time.time()
+    step_ms, fwd_ms = time_steps(step, args.warmup, args.steps, flush, world, inner=True)
+    wall = time.time() - t0
+    clock_info = clocks.stop() if clocks else None
+    fa.sync_status()
+    flops = w.fwd_flops
+    ms = max_over_ranks(statistics.mean(step_ms), world)
+    fwd_mean = max_over_ranks(statistics.mean(fwd_ms), world)
+
+    # kernel-only forward (L2 flushed) and the BF16 denominator
+    fwd_only, _ = time_steps(step_fwd_only, args.warmup, args.steps, flush, world)
+    bf16_ms, _ = time_steps(step_bf16, args.warmup, args.steps, flush, world)
+    fa.sync_status()
+    fwd_only_ms = max_over_ranks(statistics.mean(fwd_only), world)
+    bf16_mean = max_over_ranks(statistics.mean(bf16_ms), world)
+
+    # end to end through host buffers: pinned bf16 Q/K/V in, O (bf16) + LSE out
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def step_e2e(ie):
+        qd.copy_(hq, non_blocking=True)
+        kd.copy_(hk, non_blocking=True)
+        vd.copy_(hv, non_blocking=True)
+        fa.quantize(qd, fa.FMT_MXFP4, fa.ALONG_D, out=q4)
+        fa.quantize(kd, fa.FMT_MXFP4, fa.ALONG_D, out=k4)
+        fa.quantize(vd, fa.FMT_MXFP4, fa.ALONG_N, out=vt)
+        fa.fwd(q4, k4, vt, causal=False, out_dtype=fa.OUT_BF16, out=o, lse=lse)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    e2e_ms, _ = time_steps(step_e2e, args.warmup, args.steps, flush, world)
+    e2e_mean = max_over_ranks(statistics.mean(e2e_ms), world)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    # causal GQA training shape: forward + backward (if the backward is built)
+    train = None
+    try:
+        train = run_train(fa, dev, args, world)
+    except Exception as e:  # reported, not hidden
+        train = {"error": f"{type(e).__name__}: {e}"}
+
+    pk = peaks()
+    fp4_peak = pk["bf16"] * FP4_OVER_BF16
+    achieved = flops / (fwd_mean * 1e-3) / 1e12
+    result = {
+        "metric": METRIC,
+        "value": round(world * flops / (ms * 1e-3) / 1e12, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e2m1",
+        "data": "synthetic (seeded bf16 N(0,1) Q/K/V)",
+        "config": {"workload": w.name, "B": w.B, "H": w.Hq, "N": w.N, "d": w.d, "causal": False,
+                   "step": "quantize Q,K,V (MXFP4) + Direct-P FP4 forward, bf16 O + LSE",
+                   "l2": "flushed (256 MiB write) before every timed step",
+                   "parallelism": f"independent problems x{world}"},
+        "speedup_vs_bf16": round(bf16_mean / ms, 3),
+        "speedup_vs_bf16_kernel_only": round(bf16_mean / fwd_only_ms, 3),
+        "fwd_kernel_tflops": round(flops / (fwd_only_ms * 1e-3) / 1e12, 2),
+        "bf16_kernel_tflops": round(flops / (bf16_mean * 1e-3) / 1e12, 2),
+        "quantize_ms": round(ms - fwd_mean, 4),
+        "roofline": {"kernel": "fwd_fp4_kernel<128>", "bound": "tensor", "achieved": round(achieved, 1),
+                     "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 4),
+                     "traffic": None,
+                     "peak_source": f"{pk['source']} bf16 burst {pk['bf16']} TFLOP/s x nominal FP4/BF16 ratio 6"},
+        "e2e": {"value": round(world * flops / (e2e_mean * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_mean, 4)},
+        "gpu_launches": 4 * args.steps,
+        "timed_wall_s": round(wall, 3),
+        "clocks": clock_info,
+        "train": train,
+    }
+    return result
+
+
+def run_train(fa, dev, args, world):
+    w = TRAIN_8B
+    q, k, v, do = (t.to(dev) for t in make_inputs(w, seed=0, with_dout=True))
+    B, Hq, Hkv, N, d = w.B, w.Hq, w.Hkv, w.N, w.d
+    q4, k4 = fa.quantize(q), fa.quantize(k)
+    vt = fa.quantize(v, fa.FMT_MXFP4, fa.ALONG_N)
+    q8c = fa.quantize(q, fa.FMT_MXFP8, fa.ALONG_N)
+    k8c = fa.quantize(k, fa.FMT_MXFP8, fa.ALONG_N)
+    v8r = fa.quantize(v, fa.FMT_MXFP8, fa.ALONG_D)
+    o = torch.empty((B, Hq, N, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    flush = Flusher(dev)
+
+    def fwd_step(ie):
+        fa.fwd(q4, k4, vt, causal=True, out_dtype=fa.OUT_F32, out=o, lse=lse)
+
+    f_ms, _ = time_steps(fwd_step, args.warmup, args.steps, flush, world)
+    fa.sync_status()
+    out = {"workload": w.name, "fwd_ms": round(statistics.mean(f_ms), 4),
+           "fwd_tflops": round(w.fwd_flops / (statistics.mean(f_ms) * 1e-3) / 1e12, 2)}
+    ws = torch.empty(max(fa.bwd_workspace_bytes(B, Hq, Hkv, N, d), 16), dtype=torch.uint8, device=dev)
+    try:
+        fa.bwd(q4, k4, q8c, k8c, v8r, o, do, lse, causal=True, workspace=ws)
+        fa.sync_status()
+    except Exception as e:
+        out["bwd"] = f"unavailable: {e}"
+        return out
+
+    def bwd_step(ie):
+        fa.bwd(q4, k4, q8c, k8c, v8r, o, do, lse, causal=True, workspace=ws)
+
+    b_ms, _ = time_steps(bwd_step, args.warmup, args.steps, flush, world)
+    fa.sync_status()
+    bm = statistics.mean(b_ms)
+    out.update({"bwd_ms": round(bm, 4), "bwd_tflops": round(w.bwd_flops / (bm * 1e-3) / 1e12, 2)})
+    return out
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline: the oracle, as it stands, on a bounded sample
+# ----------------------------------------------------------------------------
+def oracle_sample(heads: int = 8, rows_tiles: int = 32):
+    """Quantize `heads` heads of the 4K workload and run the oracle forward for
+    `rows_tiles` 128-query tiles of each.  Returns (seconds, flops, threads)."""
+    import numpy as np
+    import oracle
+    w = FWD_4K
+    q, k, v = make_inputs(w, seed=0)
+    qf, kf, vf = (t[:1, :heads].float().numpy() for t in (q, k, v))
+    oracle.build()
+    t0 = time.time()
+    shp = qf.shape
+    Qd = oracle.dequantize(*oracle.quantize(qf, 0, 0), shp, 0, 0)
+    Kd = oracle.dequantize(*oracle.quantize(kf, 0, 0), shp, 0, 0)
+    Vd = oracle.dequantize(*oracle.quantize(vf, 0, 1), shp, 0, 1)
+    rows = np.concatenate([h * w.N + np.arange(rows_tiles * 128) for h in range(heads)])
+    oracle.fwd(Qd, Kd, Vd, rows=rows)
+    dt = time.time() - t0
+    flops = 4.0 * len(rows) * w.N * w.d
+    return dt, flops, oracle.num_threads()
+
+
+def cpu_baseline_entry():
+    dt, flops, thr = oracle_sample(heads=8, rows_tiles=32)
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+            "sample": "4K workload, 8 heads of batch 0: oracle MXFP4 quantize of Q/K/V and the Direct-P "
+                      f"forward of all 4096 query rows of each ({flops / 1e9:.1f} GFLOP in {dt:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    times = []
+    for _ in range(args.warmup):
+        oracle_sample(heads=1, rows_tiles=32)
+    flops = None
+    thr = 1
+    for _ in range(args.steps):
+        dt, flops, thr = oracle_sample(heads=1, rows_tiles=32)
+        times.append(dt)
+    mean = statistics.mean(times)
+    val = flops / mean / 1e12
+    return {"impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded bf16 N(0,1) Q/K/V)",
+            "config": {"workload": FWD_4K.name, "B": FWD_4K.B, "H": FWD_4K.Hq, "N": FWD_4K.N, "d": FWD_4K.d,
+                       "causal": False, "step": "CPU oracle on a bounded sample (see cpu_baseline.sample)"},
+            "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                             "sample": "4K workload, head 0 of batch 0: oracle quantize of Q/K/V + Direct-P forward of all 4096 query rows"},
+            "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    rank, world, local = dist_setup(args.gpus)
+    res = run_ours(args, rank, world, local)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline_entry()
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

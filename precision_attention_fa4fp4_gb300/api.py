@@ -59,7 +59,7 @@ def load_library():
         lib.fa4bf16_fwd.restype = i
         lib.fa4bf16_fwd.argtypes = [vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, vp]
         lib.fa4fp4_directp_codes.restype = i
-        lib.fa4fp4_directp_codes.argtypes = [vp, ctypes.c_int64, f, f, vp, vp]
+        lib.fa4fp4_directp_codes.argtypes = [vp, ctypes.c_int64, f, f, i, vp, vp]
         lib.fa4fp4_sync_status.restype = i
         lib.fa4fp4_sync_status.argtypes = [vp]
         _lib = lib
@@ -189,14 +189,16 @@ def bf16_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
     return out, (lse if with_lse else None)
 
 
-def directp_codes(s: torch.Tensor, m: float, c: float) -> torch.Tensor:
-    """Direct-P code of each FP32 score against max m (fa4fp4_directp_codes)."""
+def directp_codes(s: torch.Tensor, m: float, c: float, native_exp: bool = False) -> torch.Tensor:
+    """Direct-P code of each FP32 score against max m (fa4fp4_directp_codes);
+    native_exp selects the native-exponential route instead of the exact
+    threshold classifier."""
     _cuda(s)
     if s.dtype != torch.float32:
         raise ValueError("directp_codes expects float32 scores")
     out = torch.empty(s.shape, dtype=torch.uint8, device=s.device)
     _check("fa4fp4_directp_codes", load_library().fa4fp4_directp_codes(
-        _ptr(s), s.numel(), float(m), float(c), _ptr(out), _stream(s.device)))
+        _ptr(s), s.numel(), float(m), float(c), int(bool(native_exp)), _ptr(out), _stream(s.device)))
     return out
 
 

@@ -181,11 +181,11 @@ fa4fp4_status fa4fp4_fwd(const void* qc, const void* qs, const void* kc, const v
   return launch_status(launch_fwd_fp4(p, static_cast<cudaStream_t>(stream)));
 }
 
-fa4fp4_status fa4fp4_directp_codes(const float* s, int64_t n, float m, float c, uint8_t* codes,
-                                   void* stream) {
-  if (!s || !codes || n < 0) return FA4FP4_ERR_INVALID_ARG;
+fa4fp4_status fa4fp4_directp_codes(const float* s, int64_t n, float m, float c, int native_exp,
+                                   uint8_t* codes, void* stream) {
+  if (!s || !codes || n < 0 || (native_exp != 0 && native_exp != 1)) return FA4FP4_ERR_INVALID_ARG;
   if (n == 0) return FA4FP4_OK;
-  return launch_status(launch_directp_codes(s, n, m, c, directp_thresholds(), codes,
+  return launch_status(launch_directp_codes(s, n, m, c, directp_thresholds(), native_exp, codes,
                                             static_cast<cudaStream_t>(stream)));
 }
 
@@ -206,9 +206,33 @@ fa4fp4_status fa4fp4_bwd(const void*, const void*, const void*, const void*, con
   return FA4FP4_ERR_UNSUPPORTED;
 }
 
-fa4fp4_status fa4bf16_fwd(const void*, const void*, const void*, int, int, int, int, int, float,
-                          int, void*, int, float*, void*) {
-  return FA4FP4_ERR_UNSUPPORTED;
+fa4fp4_status fa4bf16_fwd(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,
+                          int N, int d, float softmax_scale, int causal, void* o, int out_dtype,
+                          float* lse, void* stream) {
+  if (!q || !k || !v || !o) return FA4FP4_ERR_INVALID_ARG;
+  if (out_dtype != FA4FP4_OUT_F32 && out_dtype != FA4FP4_OUT_BF16) return FA4FP4_ERR_INVALID_ARG;
+  fa4fp4_status s = check_dims(B, Hq, Hkv, N, d);
+  if (s != FA4FP4_OK) return s;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
+    return FA4FP4_ERR_ALIGNMENT;
+  if (B == 0 || Hq == 0) return FA4FP4_OK;
+  FwdBf16Params p;
+  memset(&p, 0, sizeof(p));
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_map(&p.tm_q, bf, 2, q, d, N, (uint64_t)B * Hq, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&p.tm_k, bf, 2, k, d, N, (uint64_t)B * Hkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&p.tm_v, bf, 2, v, d, N, (uint64_t)B * Hkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return FA4FP4_ERR_CUDA;
+  p.o = o;
+  p.lse = lse;
+  p.err = err_word();
+  if (!p.err) return FA4FP4_ERR_CUDA;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d;
+  p.causal = causal ? 1 : 0;
+  p.out_bf16 = out_dtype == FA4FP4_OUT_BF16;
+  p.scale = default_scale(softmax_scale, d);
+  p.c = (float)((double)p.scale * 1.4426950408889634);
+  return launch_status(launch_fwd_bf16(p, static_cast<cudaStream_t>(stream)));
 }
 
 fa4fp4_status fa4fp4_sync_status(void* stream) {

@@ -303,3 +303,49 @@ FA4_DEV uint32_t pack_e4m3x4(float x0, float x1, float x2, float x3) {
 FA4_DEV float exp2i(int e) { return __int_as_float((e + 127) << 23); }
 
 }  // namespace fa4
+
+namespace fa4 {
+
+// 1 column x 32 lanes TMEM load / store.
+FA4_DEV uint32_t tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+  return r;
+}
+FA4_DEV void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+// Named barrier over `nthreads` threads (whole warps).
+FA4_DEV void named_bar(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Packed FP32x2 fused multiply-add (two lanes per instruction).
+FA4_DEV float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+FA4_DEV float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// Two floats -> one byte of two E2M1 codes (RNE, satfinite); a in the low nibble.
+FA4_DEV uint32_t cvt_e2m1x2(float a, float b) {
+  uint32_t out;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n cvt.u32.u8 %0, t;\n}\n"
+      : "=r"(out)
+      : "f"(a), "f"(b));
+  return out;
+}
+
+}  // namespace fa4

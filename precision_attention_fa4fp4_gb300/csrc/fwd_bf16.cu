@@ -1,0 +1,296 @@
+// fwd_bf16.cu -- BF16 FlashAttention forward for sm_103a, the reference the
+// FP4 Direct-P forward is measured against ("Hardware-Aware FP4
+// FlashAttention-4", technical summary, Results: speedups are quoted over a
+// BF16 FlashAttention-4 baseline).
+//
+// Same CTA organisation as the FP4 kernel: one CTA per (batch*head,
+// 128-query tile); warp 0 TMA producer, warp 1 TMEM owner + tcgen05.mma
+// (kind::f16, BF16 x BF16 -> FP32) issuer, warps 2-5 softmax with one query
+// row per thread.  Exact online softmax: P = 2^(c*s - c*m) (MUFU ex2), the
+// normalizer summed from FP32 P, P rounded to BF16 for the P V product, O
+// rescaled in TMEM whenever the running max grows.
+// Q, K and P are K-major with the 128-byte swizzle (64-element chunks); V is
+// consumed MN-major straight from its row-major [keys][d] layout.
+#include <cuda_bf16.h>
+#include "common.cuh"
+#include "internal.h"
+
+namespace fa4 {
+namespace {
+
+constexpr int BM = 128, BN = 128;
+constexpr int NTHREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256;
+
+template <int D>
+struct SmemB {
+  static constexpr int STAGES = D == 128 ? 2 : 4;
+  static constexpr int CH = 128 * 128;              // one [128 rows][128 B] chunk
+  static constexpr int QB = (D / 64) * CH;          // Q tile
+  static constexpr int KB = (D / 64) * CH;          // K tile
+  static constexpr int VB = (D / 64) * CH;          // V tile [128 keys][D]
+  static constexpr int PB = 2 * CH;                 // P tile [128][128] bf16
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + QB;
+  static constexpr int OFF_V = OFF_K + STAGES * KB;
+  static constexpr int OFF_P = OFF_V + STAGES * VB;
+  static constexpr int OFF_BAR = OFF_P + PB;
+  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 1 + 1 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
+  static constexpr int BYTES = OFF_MISC + 64 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1) fwd_bf16_kernel(const __grid_constant__ FwdBf16Params p) {
+  using L = SmemB<D>;
+  constexpr int STAGES = L::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + STAGES;
+  uint64_t* s_full = kv_empty + STAGES;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_free + 2;
+  uint64_t* o_done = p_full + 1;
+  uint64_t* mma_done = o_done + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int nq = (p.N + BM - 1) / BM;
+  const int qt = p.causal ? (nq - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+  const int bh = blockIdx.y;
+  const int b = bh / p.Hq, h = bh % p.Hq;
+  const int bkv = b * p.Hkv + h / (p.Hq / p.Hkv);
+  const int q0 = qt * BM;
+  const int nk_all = (p.N + BN - 1) / BN;
+  const int nt = p.causal ? min(nk_all, qt + 1) : nk_all;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < STAGES; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
+    for (int s = 0; s < 2; ++s) { mbar_init(&s_full[s], 1); mbar_init(&s_free[s], 4); }
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      mbar_arrive_expect_tx(q_full, L::QB);
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_3d(smem + L::OFF_Q + c * L::CH, &p.tm_q, q_full, 64 * c, q0, bh);
+      int issued = 0;
+      for (int j = 0; j < nt; ++j) {
+        const int st = j % STAGES;
+        if (j >= STAGES && !mbar_wait(&kv_empty[st], ((j / STAGES) - 1) & 1, abort_flag, p.err)) break;
+        mbar_arrive_expect_tx(&kv_full[st], L::KB + L::VB);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(smem + L::OFF_K + st * L::KB + c * L::CH, &p.tm_k, &kv_full[st], 64 * c, j * BN, bkv);
+          tma_load_3d(smem + L::OFF_V + st * L::VB + c * L::CH, &p.tm_v, &kv_full[st], 64 * c, j * BN, bkv);
+        }
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        volatile int no_abort = 0;
+        for (int j = max(0, issued - STAGES); j < issued; ++j)
+          mbar_wait(&kv_full[j % STAGES], (j / STAGES) & 1, &no_abort, p.err);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_f16(BM, BN, true, false, false);
+      const uint32_t idesc_o = idesc_f16(BM, D, true, false, true);
+      const uint32_t sq = smem_u32(smem + L::OFF_Q);
+      const uint32_t sp = smem_u32(smem + L::OFF_P);
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
+      tc_fence_after();
+      auto issue_pv = [&](int t) -> bool {
+        if (!mbar_wait(p_full, t & 1, abort_flag, p.err)) return false;
+        tc_fence_after();
+        const int st = t % STAGES;
+        const uint32_t sv = smem_u32(smem + L::OFF_V + st * L::VB);
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          uint64_t ad = make_sdesc(sp + (k / 4) * L::CH + (k % 4) * 32, 16, 1024, SW_128B);
+          uint64_t bd = make_sdesc(sv + k * 16 * 128, L::CH, 1024, SW_128B);
+          mma_f16(tbase + COL_O, ad, bd, idesc_o, t > 0 || k > 0);
+        }
+        mma_commit(o_done);
+        mma_commit(&kv_empty[st]);
+        return true;
+      };
+      for (int j = 0; ok && j < nt; ++j) {
+        const int st = j % STAGES;
+        if (!mbar_wait(&kv_full[st], (j / STAGES) & 1, abort_flag, p.err)) { ok = false; break; }
+        const int sb = j & 1;
+        if (j >= 2 && !mbar_wait(&s_free[sb], ((j >> 1) - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sk = smem_u32(smem + L::OFF_K + st * L::KB);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          uint32_t off = (k / 4) * L::CH + (k % 4) * 32;
+          mma_f16(tbase + (sb ? COL_S1 : COL_S0), make_sdesc(sq + off, 16, 1024, SW_128B),
+                  make_sdesc(sk + off, 16, 1024, SW_128B), idesc_s, k > 0);
+        }
+        mma_commit(&s_full[sb]);
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok && nt > 0) issue_pv(nt - 1);
+      mma_commit(mma_done);
+      volatile int no_abort = 0;
+      mbar_wait(mma_done, 0, &no_abort, p.err);
+    }
+    __syncwarp();
+  } else {
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int qi = q0 + r;
+    const uint32_t lane_base = tbase + ((uint32_t)(quad * 32) << 16);
+    const float c = p.c;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      const int sb = j & 1;
+      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
+      tc_fence_after();
+      float s[BN];
+#pragma unroll
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + (sb ? COL_S1 : COL_S0) + cc * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(v[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
+      const int kbase = j * BN;
+      if (kbase + BN > p.N || (p.causal && kbase + BN - 1 > q0)) {
+        const int lim = p.causal ? min(p.N - 1, qi) : p.N - 1;
+#pragma unroll
+        for (int i = 0; i < BN; ++i)
+          if (kbase + i > lim) s[i] = -INFINITY;
+      }
+      float tmax = s[0];
+#pragma unroll
+      for (int i = 1; i + 1 < BN; i += 2) tmax = fmax3(tmax, s[i], s[i + 1]);
+      tmax = fmaxf(tmax, s[BN - 1]);
+      const float m_new = fmaxf(m, tmax);
+      const float mc = m_new * c;
+      uint32_t pk[BN / 2];
+      float lsum = 0.f;
+#pragma unroll
+      for (int i = 0; i < BN / 2; ++i) {
+        float p0 = ex2_approx(fmaf(s[2 * i], c, -mc));
+        float p1 = ex2_approx(fmaf(s[2 * i + 1], c, -mc));
+        lsum += p0 + p1;
+        __nv_bfloat162 t = __floats2bfloat162_rn(p0, p1);
+        pk[i] = *reinterpret_cast<uint32_t*>(&t);
+      }
+      const float alpha = (m == -INFINITY) ? 1.f : ex2_approx(fmaf(m, c, -mc));
+      if (j > 0) {
+        if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t v[32];
+            tmem_ld32(lane_base + COL_O + cc * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(lane_base + COL_O + cc * 32, v);
+          }
+          tmem_st_wait();
+        }
+      }
+      l = alpha * l + lsum;
+      m = m_new;
+      // P row r: keys 0-63 in chunk 0, 64-127 in chunk 1; 128-byte swizzle
+      uint8_t* prow = smem + L::OFF_P + r * 128;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int ch = k / 8, sub = k % 8;
+        *reinterpret_cast<uint4*>(prow + ch * L::CH + ((sub ^ (r & 7)) << 4)) =
+            make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (ok && nt > 0 && mbar_wait(o_done, (nt - 1) & 1, abort_flag, p.err)) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const bool valid = qi < p.N;
+      const long long orow = ((long long)bh * p.N + qi) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + COL_O + cc * 32, v);
+        tmem_ld_wait();
+        if (valid) {
+          if (p.out_bf16) {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow + cc * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(v[q * 8 + 2 * e]) * inv_l,
+                                                         __uint_as_float(v[q * 8 + 2 * e + 1]) * inv_l);
+                w[e] = *reinterpret_cast<uint32_t*>(&t);
+              }
+              dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + orow + cc * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv_l, __uint_as_float(v[4 * q + 1]) * inv_l,
+                                   __uint_as_float(v[4 * q + 2]) * inv_l, __uint_as_float(v[4 * q + 3]) * inv_l);
+          }
+        }
+      }
+      if (valid && p.lse) p.lse[(long long)bh * p.N + qi] = p.scale * m + logf(l);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tbase, TMEM_COLS);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16(const FwdBf16Params& p, cudaStream_t st) {
+  const int nq = (p.N + BM - 1) / BM;
+  dim3 grid(nq, p.B * p.Hq);
+  if (p.d == 128) {
+    auto k = fwd_bf16_kernel<128>;
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemB<128>::BYTES);
+    k<<<grid, NTHREADS, SmemB<128>::BYTES, st>>>(p);
+  } else {
+    auto k = fwd_bf16_kernel<64>;
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemB<64>::BYTES);
+    k<<<grid, NTHREADS, SmemB<64>::BYTES, st>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fa4

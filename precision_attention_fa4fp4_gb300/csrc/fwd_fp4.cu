@@ -3,24 +3,34 @@
 // "Hardware-Aware FP4 FlashAttention-4" (arXiv:2609.04105), technical
 // summary, Methodology 1: S = Q K^T on FP4 tensor cores; each score's offset
 // from the running row max classified straight into an E2M1 probability code
-// ("Direct Mapping"); the normalizer accumulated from the same codes the P V
+// ("Direct Mapping", by threshold comparison "or selective native
+// exponentials"); the normalizer accumulated from the same codes the P V
 // product consumes ("Consistent Normalization"); MXFP4 for P and V ("Format
 // Selection").  Q and K are MXFP4 as well.
 //
-// One CTA per (batch*head, 128-query tile), 6 warps:
-//   warp 0     producer: TMA loads of Q, K_j, V^T_j codes into swizzled shared
-//              memory; their E8M0 scales rearranged into the 32x16-byte chunks
-//              the scale-factor TMEM copy expects.
-//   warp 1     TMEM allocation; one elected lane issues tcgen05.cp for scale
-//              factors and tcgen05.mma (kind::mxf4, block_scale) for
-//              S_j = Q K_j^T into a double-buffered S and O += P_j V_j.
-//   warps 2-5  softmax: one query row per thread (TMEM lane quadrant =
-//              warp % 4).  Row max, Direct-P codes, code-sum normalizer, the
-//              eager O rescale in TMEM, packed P codes to shared memory.
-// The QK^T of tile j+1 runs on the tensor core while tile j's codes are built.
+// One CTA per (batch*head, 128-query tile), 18 warps:
+//   warp 0      producer: TMA loads of Q, K_j, V^T_j codes into swizzled shared
+//               memory; their E8M0 scales rearranged into the 32x16-byte chunks
+//               the scale-factor TMEM copy expects.
+//   warp 1      TMEM allocation; one lane issues tcgen05.cp (scale factors) and
+//               tcgen05.mma kind::mxf4 block_scale: S_j = Q K_j^T into a
+//               double-buffered S, O += P_j V_j, and l += P_j 1 (an N=16 MMA
+//               against an all-ones E2M1 tile, so the normalizer is summed by
+//               the tensor core from exactly the codes P V consumes).
+//   warps 2-17  softmax: 4 warps per TMEM lane quadrant; thread (row r, column
+//               group g) owns S[r][32g, 32g+32).  Row max exchanged through
+//               shared memory (one mbarrier per quadrant), Direct-P codes,
+//               eager O rescale of its 32 O columns, one 16-byte P chunk.
+// QK^T of tile j+1 runs on the tensor core while tile j's codes are built.
 #include <cuda_bf16.h>
 #include "common.cuh"
 #include "internal.h"
+
+// Columns of each thread's 32 that take the native-exponential route
+// (ex2 + RNE to E2M1); the rest take the exact threshold classifier.
+#ifndef FA4_NATIVE_PER_32
+#define FA4_NATIVE_PER_32 24
+#endif
 
 namespace fa4 {
 namespace {
@@ -28,10 +38,13 @@ namespace {
 constexpr int BM = 128;         // queries per CTA
 constexpr int BN = 128;         // keys per tile
 constexpr int STAGES = 6;       // K/V pipeline depth
-constexpr int NTHREADS = 192;
+constexpr int NSOFT = 16;       // softmax warps
+constexpr int NTHREADS = 32 * (2 + NSOFT);
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_SFQ = 384, COL_SFP = 388,
-                   COL_SFK = 392, COL_SFV = 392 + 4 * STAGES;
+constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_L = 384, COL_SFQ = 400,
+                   COL_SFP = 404, COL_SFK = 408, COL_SFV = 408 + 4 * STAGES;
+static_assert(COL_SFV + 4 * STAGES <= TMEM_COLS, "TMEM budget");
+constexpr float LOG2_6 = 2.5849625007211562f;
 
 template <int D>
 struct Smem {
@@ -39,15 +52,18 @@ struct Smem {
   static constexpr int KB = BN * D / 2;
   static constexpr int VB = D * BN / 2;   // V^T: D rows of 128 keys
   static constexpr int PB = BM * BN / 2;
+  static constexpr int ONESB = 16 * 64;   // 16 rows of 128 E2M1 ones
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + QB;
   static constexpr int OFF_V = OFF_K + STAGES * KB;
   static constexpr int OFF_P = OFF_V + STAGES * VB;
-  static constexpr int OFF_SF = OFF_P + 2 * PB;           // 512-byte scale chunks
+  static constexpr int OFF_ONES = OFF_P + 2 * PB;
+  static constexpr int OFF_SF = OFF_ONES + ONESB;         // 512-byte scale chunks
   static constexpr int SF_Q = OFF_SF, SF_P = SF_Q + 512, SF_K = SF_P + 512,
                        SF_V = SF_K + 512 * STAGES;
-  static constexpr int OFF_BAR = SF_V + 512 * STAGES;
-  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 1 + 1 + 1;
+  static constexpr int OFF_RED = SF_V + 512 * STAGES;     // float [2][4][128]
+  static constexpr int OFF_BAR = OFF_RED + 2 * 4 * 128 * 4;
+  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 1 + 1 + 1 + 8;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int BYTES = OFF_MISC + 64 + 1024;    // + alignment slack
 };
@@ -60,12 +76,25 @@ FA4_DEV uint32_t directp_code(float x, const float (&T)[7]) {
   return c;
 }
 
-// Sum of E2M1 magnitudes (times 2) of the 8 codes packed in w.
-FA4_DEV uint32_t code_sum2(uint32_t w, uint32_t acc) {
-  const uint32_t lo = 0x03020100u, hi = 0x0C080604u;   // 2*{0,.5,1,1.5,2,3,4,6}
-  acc = __dp4a(__byte_perm(lo, hi, w & 0xffffu), 0x01010101u, acc);
-  acc = __dp4a(__byte_perm(lo, hi, w >> 16), 0x01010101u, acc);
-  return acc;
+// Codes of 8 consecutive scores, packed (element e in nibble e).
+// native: RNE_E2M1(2^(x + log2 6)) via MUFU ex2; exact: threshold count.
+template <bool NATIVE>
+FA4_DEV uint32_t codes8(const float* s, float c, float mc, float bias, const float (&T)[7]) {
+  uint32_t w = 0;
+  if (NATIVE) {
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      float2 x = ffma2(make_float2(s[e], s[e + 1]), make_float2(c, c), make_float2(bias, bias));
+      w |= cvt_e2m1x2(ex2_approx(x.x), ex2_approx(x.y)) << (4 * e);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      float2 x = ffma2(make_float2(s[e], s[e + 1]), make_float2(c, c), make_float2(-mc, -mc));
+      w |= (directp_code(x.x, T) | (directp_code(x.y, T) << 4)) << (4 * e);
+    }
+  }
+  return w;
 }
 
 // Rearrange 128 rows of per-row scale words into the scale-factor chunk:
@@ -101,8 +130,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
   uint64_t* p_full = s_free + 2;
   uint64_t* o_done = p_full + 1;
   uint64_t* mma_done = o_done + 1;
+  uint64_t* red_bar = mma_done + 1;          // [2 parities][4 quadrants]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+  float* red = reinterpret_cast<float*>(smem + L::OFF_RED);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nq = (p.N + BM - 1) / BM;
@@ -117,16 +148,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < STAGES; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
-    for (int s = 0; s < 2; ++s) { mbar_init(&s_full[s], 1); mbar_init(&s_free[s], 4); }
-    mbar_init(p_full, 4);
+    for (int s = 0; s < 2; ++s) { mbar_init(&s_full[s], 1); mbar_init(&s_free[s], NSOFT); }
+    mbar_init(p_full, NSOFT);
     mbar_init(o_done, 1);
     mbar_init(mma_done, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&red_bar[i], 128);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
-    // unit E8M0 scale (byte 127) for every P block
+    // unit E8M0 scale (byte 127) for every P block and the ones tile; the
+    // ones tile holds E2M1 1.0 (code 2) in every nibble
     reinterpret_cast<uint4*>(smem + L::SF_P)[lane] = make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
+    reinterpret_cast<uint4*>(smem + L::OFF_ONES)[lane] = make_uint4(0x22222222u, 0x22222222u, 0x22222222u, 0x22222222u);
+    reinterpret_cast<uint4*>(smem + L::OFF_ONES)[lane + 32] = make_uint4(0x22222222u, 0x22222222u, 0x22222222u, 0x22222222u);
     fence_proxy_async_smem();
     tmem_alloc(tmem_holder, TMEM_COLS);
   }
@@ -157,7 +192,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       const int st = j % STAGES;
       if (j >= STAGES && !mbar_wait(&kv_empty[st], ((j / STAGES) - 1) & 1, abort_flag, p.err)) break;
       stage_sf_rows(smem + L::SF_K + 512 * st, ks, j * BN, min(BN, p.N - j * BN), D / 32, lane);
-      // V^T scales: channel rows, 4 key blocks of tile j
       {
         uint32_t w[4];
 #pragma unroll
@@ -176,7 +210,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       }
       issued = j + 1;
     }
-    // drain: never leave a bulk copy in flight into this CTA's shared memory
     if (*abort_flag && lane == 0) {
       volatile int no_abort = 0;
       for (int j = max(0, issued - STAGES); j < issued; ++j)
@@ -188,9 +221,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       constexpr int KSTEPS = D / 64;   // K = 64 per mxf4 MMA
       const uint32_t idesc_s = idesc_bs(BM, BN, 1, 1, false, false, 0, 0);
       const uint32_t idesc_o = idesc_bs(BM, D, 1, 1, false, false, 0, 0);
+      const uint32_t idesc_l = idesc_bs(BM, 16, 1, 1, false, false, 0, 0);
       constexpr Swizzle QSW = D == 128 ? SW_64B : SW_32B;
       constexpr uint32_t QSBO = D == 128 ? 512 : 256;
       const uint32_t sq = smem_u32(smem + L::OFF_Q);
+      const uint32_t sones = smem_u32(smem + L::OFF_ONES);
       bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
       tc_fence_after();
       if (ok) {
@@ -205,10 +240,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
         const uint32_t sv = smem_u32(smem + L::OFF_V + st * L::VB);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {     // 128 keys = 2 x K64
-          uint64_t ad = make_sdesc(sp + 32 * k, 16, 512, SW_64B);
-          uint64_t bd = make_sdesc(sv + 32 * k, 16, 512, SW_64B);
-          uint32_t id = idesc_o | ((uint32_t)(2 * k) << 29) | ((uint32_t)(2 * k) << 4);
-          mma_mxf4(tbase + COL_O, ad, bd, id, tbase + COL_SFP, tbase + COL_SFV + 4 * st, t > 0 || k > 0);
+          const uint64_t ad = make_sdesc(sp + 32 * k, 16, 512, SW_64B);
+          const uint32_t sf = ((uint32_t)(2 * k) << 29) | ((uint32_t)(2 * k) << 4);
+          mma_mxf4(tbase + COL_O, ad, make_sdesc(sv + 32 * k, 16, 512, SW_64B), idesc_o | sf,
+                   tbase + COL_SFP, tbase + COL_SFV + 4 * st, t > 0 || k > 0);
+          mma_mxf4(tbase + COL_L, ad, make_sdesc(sones + 32 * k, 16, 512, SW_64B), idesc_l | sf,
+                   tbase + COL_SFP, tbase + COL_SFP, t > 0 || k > 0);
         }
         mma_commit(o_done);
         mma_commit(&kv_empty[st]);
@@ -235,7 +272,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
       if (ok && nt > 0) issue_pv(nt - 1);
-      // all tcgen05 work of this thread completes before TMEM is released
       mma_commit(mma_done);
       volatile int no_abort = 0;
       mbar_wait(mma_done, 0, &no_abort, p.err);
@@ -244,6 +280,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
   } else {
     // ------------------------------------------------------------ softmax
     const int quad = warp & 3;
+    const int g = (warp - 2) >> 2;            // column group 0..3
     const int r = quad * 32 + lane;
     const int qi = q0 + r;
     const uint32_t lane_base = tbase + ((uint32_t)(quad * 32) << 16);
@@ -251,74 +288,78 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
     float T[7];
 #pragma unroll
     for (int k = 0; k < 7; ++k) T[k] = p.T[k];
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY;
     bool ok = true;
-    uint8_t* prow_base = smem + L::OFF_P + r * 64;
+    const int x = (r >> 1) & 3;               // 64-byte swizzle phase of row r
+    uint8_t* pchunk = smem + L::OFF_P + r * 64 + ((g ^ x) << 4);
     for (int j = 0; j < nt; ++j) {
       const int sb = j & 1;
       if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
       tc_fence_after();
-      float s[BN];
-#pragma unroll
-      for (int cc = 0; cc < BN / 32; ++cc) {
+      float s[32];
+      {
         uint32_t v[32];
-        tmem_ld32(lane_base + (sb ? COL_S1 : COL_S0) + cc * 32, v);
+        tmem_ld32(lane_base + (sb ? COL_S1 : COL_S0) + 32 * g, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(v[i]);
+        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(v[i]);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[sb]);
-      const int kbase = j * BN;
-      if (kbase + BN > p.N || (p.causal && kbase + BN - 1 > q0)) {
+      const int kbase = j * BN + 32 * g;
+      if (j * BN + BN > p.N || (p.causal && j * BN + BN - 1 > q0)) {
         const int lim = p.causal ? min(p.N - 1, qi) : p.N - 1;
 #pragma unroll
-        for (int i = 0; i < BN; ++i)
+        for (int i = 0; i < 32; ++i)
           if (kbase + i > lim) s[i] = -INFINITY;
       }
-      float tmax = s[0];
+      float pm = fmax3(s[0], s[1], s[2]);
 #pragma unroll
-      for (int i = 1; i + 1 < BN; i += 2) tmax = fmax3(tmax, s[i], s[i + 1]);
-      tmax = fmaxf(tmax, s[BN - 1]);
+      for (int i = 3; i + 1 < 32; i += 2) pm = fmax3(pm, s[i], s[i + 1]);
+      pm = fmaxf(pm, s[31]);
+      float* rslot = red + (sb * 4) * 128;
+      rslot[g * 128 + r] = pm;
+      mbar_arrive(&red_bar[sb * 4 + quad]);
+      if (!mbar_wait(&red_bar[sb * 4 + quad], (j >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
+      const float tmax = fmaxf(fmaxf(rslot[r], rslot[128 + r]), fmaxf(rslot[256 + r], rslot[384 + r]));
       const float m_new = fmaxf(m, tmax);
       const float mc = m_new * c;
-      uint32_t pw[BN / 8];
-      uint32_t acc = 0;
+      const float bias = LOG2_6 - mc;
+      uint32_t pw[4];
 #pragma unroll
-      for (int w = 0; w < BN / 8; ++w) {
-        uint32_t word = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) word |= directp_code(fmaf(s[w * 8 + e], c, -mc), T) << (4 * e);
-        pw[w] = word;
-        acc = code_sum2(word, acc);
+      for (int w = 0; w < 4; ++w) {
+        if (w * 8 < FA4_NATIVE_PER_32) pw[w] = codes8<true>(s + 8 * w, c, mc, bias, T);
+        else pw[w] = codes8<false>(s + 8 * w, c, mc, bias, T);
       }
       const float alpha = (m == -INFINITY) ? 1.f : ex2_approx(fmaf(m, c, -mc));
       if (j > 0) {
         if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
+          if (32 * g < D) {
             uint32_t v[32];
-            tmem_ld32(lane_base + COL_O + cc * 32, v);
+            tmem_ld32(lane_base + COL_O + 32 * g, v);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st32(lane_base + COL_O + cc * 32, v);
+            for (int i = 0; i < 32; i += 2) {
+              float2 t = fmul2(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                               make_float2(alpha, alpha));
+              v[i] = __float_as_uint(t.x);
+              v[i + 1] = __float_as_uint(t.y);
+            }
+            tmem_st32(lane_base + COL_O + 32 * g, v);
+          }
+          if (g == 0) {
+            uint32_t lv = tmem_ld1(lane_base + COL_L);
+            tmem_ld_wait();
+            tmem_st1(lane_base + COL_L, __float_as_uint(__uint_as_float(lv) * alpha));
           }
           tmem_st_wait();
         }
       }
-      l = alpha * l + 0.5f * (float)acc;
       m = m_new;
-      // packed codes of this row -> P[j&1], 64-byte row, 64B swizzle
-      uint8_t* prow = prow_base + sb * L::PB;
-      const int x = (r >> 1) & 3;
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        *reinterpret_cast<uint4*>(prow + ((k ^ x) << 4)) =
-            make_uint4(pw[4 * k], pw[4 * k + 1], pw[4 * k + 2], pw[4 * k + 3]);
+      *reinterpret_cast<uint4*>(pchunk + sb * L::PB) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -326,17 +367,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
     }
     if (ok && nt > 0 && mbar_wait(o_done, (nt - 1) & 1, abort_flag, p.err)) {
       tc_fence_after();
+      const float l = __uint_as_float(tmem_ld1(lane_base + COL_L));
+      tmem_ld_wait();
       const float inv_l = 1.f / l;
       const bool valid = qi < p.N;
-      const long long orow = ((long long)bh * p.N + qi) * D;
-#pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
+      const long long orow = ((long long)bh * p.N + qi) * D + 32 * g;
+      if (32 * g < D) {
         uint32_t v[32];
-        tmem_ld32(lane_base + COL_O + cc * 32, v);
+        tmem_ld32(lane_base + COL_O + 32 * g, v);
         tmem_ld_wait();
         if (valid) {
           if (p.out_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow + cc * 32);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint32_t w[4];
@@ -349,7 +391,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
               dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
             }
           } else {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + orow + cc * 32);
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + orow);
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv_l, __uint_as_float(v[4 * q + 1]) * inv_l,
@@ -357,7 +399,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
           }
         }
       }
-      if (valid && p.lse) p.lse[(long long)bh * p.N + qi] = p.scale * m + logf(l * (1.f / 6.f));
+      if (g == 0 && valid && p.lse) p.lse[(long long)bh * p.N + qi] = p.scale * m + logf(l * (1.f / 6.f));
     }
   }
   tc_fence_before();
@@ -365,15 +407,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
   if (warp == 1) tmem_dealloc(tbase, TMEM_COLS);
 }
 
+template <bool NATIVE>
 __global__ void directp_codes_kernel(const float* __restrict__ s, long long n, float m, float c,
                                      Thresh T, uint8_t* __restrict__ out) {
   float t[7];
 #pragma unroll
   for (int k = 0; k < 7; ++k) t[k] = T.v[k];
   const float mc = m * c;
+  const float bias = LOG2_6 - mc;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x)
-    out[i] = (uint8_t)directp_code(fmaf(s[i], c, -mc), t);
+       i += (long long)gridDim.x * blockDim.x) {
+    uint32_t code;
+    if (NATIVE) code = cvt_e2m1x2(ex2_approx(fmaf(s[i], c, bias)), 0.f) & 0xfu;
+    else code = directp_code(fmaf(s[i], c, -mc), t);
+    out[i] = (uint8_t)code;
+  }
 }
 
 }  // namespace
@@ -394,12 +442,13 @@ cudaError_t launch_fwd_fp4(const FwdFp4Params& p, cudaStream_t st) {
 }
 
 cudaError_t launch_directp_codes(const float* s, long long n, float m, float c, const float* T,
-                                 uint8_t* codes, cudaStream_t st) {
+                                 int native, uint8_t* codes, cudaStream_t st) {
   Thresh t;
   for (int k = 0; k < 7; ++k) t.v[k] = T[k];
   long long blocks = (n + 255) / 256;
   int grid = (int)(blocks < 152 * 16 ? (blocks > 0 ? blocks : 1) : 152 * 16);
-  directp_codes_kernel<<<grid, 256, 0, st>>>(s, n, m, c, t, codes);
+  if (native) directp_codes_kernel<true><<<grid, 256, 0, st>>>(s, n, m, c, t, codes);
+  else directp_codes_kernel<false><<<grid, 256, 0, st>>>(s, n, m, c, t, codes);
   return cudaGetLastError();
 }
 

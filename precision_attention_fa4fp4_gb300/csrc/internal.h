@@ -32,7 +32,7 @@ struct FwdFp4Params {
 };
 cudaError_t launch_fwd_fp4(const FwdFp4Params& p, cudaStream_t st);
 cudaError_t launch_directp_codes(const float* s, long long n, float m, float c, const float* T,
-                                 uint8_t* codes, cudaStream_t st);
+                                 int native, uint8_t* codes, cudaStream_t st);
 
 // ---------------------------------------------------------------- BF16 fwd
 struct FwdBf16Params {

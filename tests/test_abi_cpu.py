@@ -61,7 +61,8 @@ def test_argument_errors_before_launch(lib):
     assert lib.fa4fp4_fwd(*args, 1, 4, 4, 64, 64, 0.0, 0, p, 7, null, null) == INVALID # dtype
     assert lib.fa4fp4_fwd(*([p] * 5 + [odd]), 1, 4, 4, 64, 64, 0.0, 0, p, 1, null, null) == ALIGN
     assert lib.fa4bf16_fwd(null, p, p, 1, 1, 1, 64, 64, 0.0, 0, p, 1, null, null) == INVALID
-    assert lib.fa4fp4_directp_codes(null, 10, 0.0, 1.0, p, null) == INVALID
+    assert lib.fa4fp4_directp_codes(null, 10, 0.0, 1.0, 0, p, null) == INVALID
+    assert lib.fa4fp4_directp_codes(p, 10, 0.0, 1.0, 2, p, null) == INVALID
     assert lib.fa4fp4_status_string(5).decode() == "device pipeline wait timed out"
 
 

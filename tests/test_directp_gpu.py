@@ -35,3 +35,22 @@ def test_random_scores_and_maxima():
         got = fa.directp_codes(torch.from_numpy(s).cuda(), float(m), float(c)).cpu().numpy()
         want = np.array([oracle.directp_code(float(v), float(m), float(c)) for v in s[:3000]])
         assert np.array_equal(got[:3000], want)
+
+
+def test_native_exponential_route_close_to_exact_map():
+    """The native-exponential route (ex2 + RNE to E2M1) may differ from the
+    exact threshold map only for offsets within the hardware exp2 error of a
+    threshold: every disagreement must lie within 2e-6 of some T_k and differ
+    by one code, and disagreements must be rare."""
+    fa = require_gpu()
+    neg = np.arange(np.float32(2.0 ** -8).view(np.int32), np.float32(6.0).view(np.int32) + 1, 7, dtype=np.int32)
+    x = -(neg.view(np.float32))
+    got = fa.directp_codes(torch.from_numpy(x).cuda(), 0.0, 1.0, native_exp=True).cpu().numpy()
+    want = oracle.directp_codes_of_x(x)
+    bad = np.nonzero(got != want)[0]
+    T = oracle.directp_thresholds().astype(np.float64)
+    if bad.size:
+        dist = np.min(np.abs(x[bad, None].astype(np.float64) - T[None, :]), axis=1)
+        assert np.max(dist) < 2e-6, f"far disagreement at x={x[bad[np.argmax(dist)]]}"
+        assert np.max(np.abs(got[bad].astype(int) - want[bad].astype(int))) == 1
+    assert bad.size <= 1e-5 * x.size, f"{bad.size} of {x.size} codes differ"
