@@ -199,11 +199,73 @@ size_t fa4fp4_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
          up((size_t)B * Hq * d * Np / 32) + up(rows * sizeof(float));
 }
 
-fa4fp4_status fa4fp4_bwd(const void*, const void*, const void*, const void*, const void*,
-                         const void*, const void*, const void*, const void*, const void*,
-                         const void*, int, const void*, const float*, int, int, int, int, int,
-                         float, int, float*, float*, float*, void*, size_t, void*) {
-  return FA4FP4_ERR_UNSUPPORTED;
+fa4fp4_status fa4fp4_bwd(const void* q4c, const void* q4s, const void* k4c, const void* k4s,
+                         const void* q8c, const void* q8s, const void* k8c, const void* k8s,
+                         const void* v8c, const void* v8s, const void* o, int o_dtype,
+                         const void* dout, const float* lse, int B, int Hq, int Hkv, int N, int d,
+                         float softmax_scale, int causal, float* dq, float* dk, float* dv,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  const void* ptrs[] = {q4c, q4s, k4c, k4s, q8c, q8s, k8c, k8s, v8c, v8s, o, dout, lse, dq, dk, dv};
+  for (const void* ptr : ptrs)
+    if (!ptr) return FA4FP4_ERR_INVALID_ARG;
+  if (o_dtype != FA4FP4_OUT_F32 && o_dtype != FA4FP4_OUT_BF16) return FA4FP4_ERR_INVALID_ARG;
+  fa4fp4_status s = check_dims(B, Hq, Hkv, N, d);
+  if (s != FA4FP4_OK) return s;
+  if (d != 128) return FA4FP4_ERR_UNSUPPORTED;
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return FA4FP4_ERR_ALIGNMENT;
+  if (B == 0 || Hq == 0) return FA4FP4_OK;
+  const size_t need = fa4fp4_bwd_workspace_bytes(B, Hq, Hkv, N, d);
+  if (!workspace || workspace_bytes < need) return FA4FP4_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return FA4FP4_ERR_ALIGNMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int Np = padded_n(N);
+  const size_t rows = (size_t)B * Hq * N;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  uint8_t* do_r = w;           w += up(rows * d);
+  uint8_t* do_r_s = w;         w += up(rows * d / 32);
+  uint8_t* do_c = w;           w += up((size_t)B * Hq * d * Np);
+  uint8_t* do_c_s = w;         w += up((size_t)B * Hq * d * Np / 32);
+  float* Dvec = reinterpret_cast<float*>(w);
+
+  BwdPrepParams pp;
+  pp.o = o; pp.dout = dout; pp.o_bf16 = o_dtype == FA4FP4_OUT_BF16;
+  pp.B = B; pp.Hq = Hq; pp.N = N; pp.d = d; pp.Np = Np;
+  pp.do_r = do_r; pp.do_r_s = do_r_s; pp.do_c = do_c; pp.do_c_s = do_c_s; pp.Dvec = Dvec; pp.dq = dq;
+  cudaError_t e = launch_bwd_prep(pp, st);
+  if (e != cudaSuccess) return FA4FP4_ERR_CUDA;
+
+  BwdParams p;
+  memset(&p, 0, sizeof(p));
+  const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const uint64_t BHq = (uint64_t)B * Hq, BHk = (uint64_t)B * Hkv;
+  if (!make_map(&p.tm_k4, u8, 1, k4c, d / 2, N, BHk, d / 2, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map(&p.tm_v8r, u8, 1, v8c, d, N, BHk, d, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&p.tm_k8c, u8, 1, k8c, Np, d, BHk, 128, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&p.tm_q4, u8, 1, q4c, d / 2, N, BHq, d / 2, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map(&p.tm_do_r, u8, 1, do_r, d, N, BHq, d, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&p.tm_q8c, u8, 1, q8c, Np, d, BHq, 64, d, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map(&p.tm_do_c, u8, 1, do_c, Np, d, BHq, 64, d, CU_TENSOR_MAP_SWIZZLE_64B))
+    return FA4FP4_ERR_CUDA;
+  p.q4_s = static_cast<const uint8_t*>(q4s);
+  p.k4_s = static_cast<const uint8_t*>(k4s);
+  p.q8c_s = static_cast<const uint8_t*>(q8s);
+  p.k8c_s = static_cast<const uint8_t*>(k8s);
+  p.v8r_s = static_cast<const uint8_t*>(v8s);
+  p.do_r_s = do_r_s;
+  p.do_c_s = do_c_s;
+  p.lse = lse;
+  p.Dvec = Dvec;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  p.err = err_word();
+  if (!p.err) return FA4FP4_ERR_CUDA;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.Np = Np;
+  p.causal = causal ? 1 : 0;
+  p.scale = default_scale(softmax_scale, d);
+  p.c = (float)((double)p.scale * 1.4426950408889634);
+  p.l2e = (float)1.4426950408889634;
+  return launch_status(launch_bwd_main(p, st));
 }
 
 fa4fp4_status fa4bf16_fwd(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,

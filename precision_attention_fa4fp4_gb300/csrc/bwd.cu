@@ -1,0 +1,478 @@
+// bwd.cu -- quantized attention backward for sm_103a.
+//
+// "Hardware-Aware FP4 FlashAttention-4" (arXiv:2609.04105), technical
+// summary, Methodology 2 ("Quantized Causal Backward"): the forward saves the
+// quantized Q/K payload, scales and the LSE; the backward rebuilds P from
+// them instead of a BF16 score path ("Reconstruction") and the gradient
+// products consume row/column-oriented FP8 views of Q, K, V ("Gradient
+// Formats"); the abstract adds FP8 gradient operands for P, dS and dO.
+//
+// bwd_prep_kernel: D_i = sum_t dO_it O_it and zeroes dq (the main kernel
+//   accumulates dq with atomics).  The MXFP8 views of dO come from the
+//   quantize kernels.
+// bwd_kernel: one CTA per (batch, kv head, 128-key tile); loop over the query
+//   heads of the GQA group x 64-query tiles (causal: from the diagonal on).
+//   warp 0       producer (TMA + scale-chunk staging + LSE/D of the tile)
+//   warp 1       TMEM owner + tcgen05 issuer:
+//                  S^T  = K4 Q4^T          kind::mxf4      M=128 keys, N=64
+//                  dP^T = V8r dOr^T        kind::mxf8f6f4  M=128 keys, N=64
+//                  dV  += Pq^T dOc         M=128 keys, N=d, K=64 queries
+//                  dK  += dSc^T Q8c        M=128 keys, N=d
+//                  dQ^T = K8c^T dSr        M=d, N=64 queries, K=128 keys
+//                                          (B operand MN-major)
+//   warps 2-9    one key row x 32 queries per thread: P = 2^(fmaf(s, c,
+//                -fl32(LSE log2 e))), dS = P (dP - D), quantized to MXFP8:
+//                P and dS in blocks of 32 queries (thread-local), dS in
+//                blocks of 32 keys (warp-wide max with redux.sync).
+//   warps 10-13  dQ^T from TMEM, times softmax_scale, added into dq.
+//   After the loop: dV and dK * softmax_scale written by warps 2-9.
+#include <cuda_bf16.h>
+#include "common.cuh"
+#include "internal.h"
+
+namespace fa4 {
+namespace {
+
+constexpr int BK = 128;          // keys per CTA
+constexpr int BQ = 64;           // queries per step
+constexpr int D = 128;
+constexpr int NTHREADS = 14 * 32;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_ST = 0, COL_DPT = 64, COL_DQT = 128, COL_DV = 192, COL_DK = 320,
+                   SF_K4 = 448, SF_V8 = 452, SF_K8 = 456, SF_P = 460, SF_DSC = 464, SF_DSR = 468,
+                   SF_Q4 = 472, SF_DOR = 480, SF_Q8 = 488, SF_DOC = 496;   // last four: [2 stages]
+static_assert(SF_DOC + 8 <= TMEM_COLS, "TMEM budget");
+
+struct BL {   // shared-memory layout (bytes)
+  static constexpr int K4 = 0;                       // 128 keys x 64 B (E2M1, d=128)
+  static constexpr int V8 = K4 + BK * D / 2;         // 128 keys x 128 B (E4M3)
+  static constexpr int K8 = V8 + BK * D;             // 128 d-rows x 128 keys (E4M3)
+  static constexpr int STG = K8 + D * BK;            // stages
+  static constexpr int Q4 = 0, DOR = Q4 + BQ * D / 2, Q8 = DOR + BQ * D, DOC = Q8 + D * BQ;
+  static constexpr int STAGE_BYTES = DOC + D * BQ;   // 28 KB
+  static constexpr int PQ = STG + 2 * STAGE_BYTES;   // 128 keys x 64 B
+  static constexpr int DSC = PQ + BK * BQ;
+  static constexpr int DSR = DSC + BK * BQ;
+  static constexpr int SFC = DSR + BK * BQ;          // scale chunks, 512 B each
+  // chunk ids: 0 K4, 1 V8, 2 K8, 3 P, 4 dSc, 5 dSr, 6-7 Q4, 8-9 dOr, 10-11 Q8, 12-13 dOc
+  static constexpr int VEC = SFC + 14 * 512;         // float lse2[2][64], dvec[2][64]
+  static constexpr int BAR = VEC + 4 * BQ * 4;
+  static constexpr int NBAR = 1 + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 1;
+  static constexpr int MISC = BAR + 8 * NBAR;
+  static constexpr int BYTES = MISC + 64 + 1024;
+};
+
+FA4_DEV int e4m3_block_exp(float amax, float* inv) {
+  int E = (int)((__float_as_uint(amax) >> 23) & 0xff);
+  int X = E - 127 - 8;
+  X = X < -127 ? -127 : (X > 127 ? 127 : X);
+  *inv = __uint_as_float((uint32_t)(127 - X) << 23);
+  return X;
+}
+
+// scale words of `nrows` rows, `bpr` bytes each (<= 4), into a chunk
+FA4_DEV void stage_chunk(uint8_t* chunk, const uint8_t* src, long long stride, int nvalid,
+                         int bpr, int lane) {
+  uint32_t w[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    int r = lane + 32 * c;
+    uint32_t v = 0;
+    if (r < nvalid) {
+      const uint8_t* p = src + r * stride;
+      v = bpr == 4 ? *reinterpret_cast<const uint32_t*>(p) : (uint32_t)*reinterpret_cast<const uint16_t*>(p);
+    }
+    w[c] = v;
+  }
+  *reinterpret_cast<uint4*>(chunk + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// 32 floats * inv -> 32 E4M3 codes as two uint4 (element 0 in byte 0)
+FA4_DEV void e4m3x32(const float* v, float inv, uint4& lo, uint4& hi) {
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w[i] = pack_e4m3x4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+  lo = make_uint4(w[0], w[1], w[2], w[3]);
+  hi = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// two 16-byte chunks 2g, 2g+1 of row r of a [rows][64 B] SW64 tile
+FA4_DEV void st_row_sw64(uint8_t* tile, int r, int g, uint4 lo, uint4 hi) {
+  const int x = (r >> 1) & 3;
+  uint8_t* row = tile + r * 64;
+  *reinterpret_cast<uint4*>(row + (((2 * g) ^ x) << 4)) = lo;
+  *reinterpret_cast<uint4*>(row + (((2 * g + 1) ^ x) << 4)) = hi;
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BL::BAR);
+  uint64_t* fix_full = bars;
+  uint64_t* in_full = bars + 1;
+  uint64_t* in_empty = bars + 3;
+  uint64_t* s_full = bars + 5;
+  uint64_t* p_full = bars + 6;
+  uint64_t* dq_full = bars + 7;
+  uint64_t* dq_free = bars + 8;
+  uint64_t* acc_done = bars + 9;
+  uint64_t* mma_done = bars + 10;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + BL::MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + BL::MISC + 4);
+  uint8_t* sfc = smem + BL::SFC;
+  float* lse2 = reinterpret_cast<float*>(smem + BL::VEC);     // [2][64]
+  float* dvec = lse2 + 2 * BQ;                                 // [2][64]
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int kt = blockIdx.x;
+  const int bkv = blockIdx.y;
+  const int b = bkv / p.Hkv, hk = bkv % p.Hkv;
+  const int group = p.Hq / p.Hkv;
+  const int k0 = kt * BK;
+  const int nqt = (p.N + BQ - 1) / BQ;
+  const int i0 = p.causal ? k0 / BQ : 0;
+  const int per_head = nqt - i0;
+  const int nsteps = group * per_head;
+
+  if (threadIdx.x == 0) {
+    mbar_init(fix_full, 1);
+    for (int s = 0; s < 2; ++s) { mbar_init(&in_full[s], 1); mbar_init(&in_empty[s], 1); }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 8);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_free, 4);
+    mbar_init(acc_done, 1);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const int nk_valid = min(BK, p.N - k0);
+    stage_chunk(sfc + 0 * 512, p.k4_s + ((long long)bkv * p.N + k0) * (D / 32), D / 32, nk_valid, 4, lane);
+    stage_chunk(sfc + 1 * 512, p.v8r_s + ((long long)bkv * p.N + k0) * (D / 32), D / 32, nk_valid, 4, lane);
+    stage_chunk(sfc + 2 * 512, p.k8c_s + (long long)bkv * D * (p.Np / 32) + k0 / 32, p.Np / 32, D, 4, lane);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive_expect_tx(fix_full, BK * D / 2 + BK * D + D * BK);
+      tma_load_3d(smem + BL::K4, &p.tm_k4, fix_full, 0, k0, bkv);
+      tma_load_3d(smem + BL::V8, &p.tm_v8r, fix_full, 0, k0, bkv);
+      tma_load_3d(smem + BL::K8, &p.tm_k8c, fix_full, k0, 0, bkv);
+    }
+    int issued = 0;
+    for (int t = 0; t < nsteps; ++t) {
+      const int st = t & 1;
+      const int h = hk * group + t / per_head;
+      const int q0 = (i0 + t % per_head) * BQ;
+      const int bh = b * p.Hq + h;
+      if (t >= 2 && !mbar_wait(&in_empty[st], ((t >> 1) - 1) & 1, abort_flag, p.err)) break;
+      const int nq_valid = min(BQ, p.N - q0);
+      stage_chunk(sfc + (6 + st) * 512, p.q4_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, 4, lane);
+      stage_chunk(sfc + (8 + st) * 512, p.do_r_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, 4, lane);
+      stage_chunk(sfc + (10 + st) * 512, p.q8c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
+      stage_chunk(sfc + (12 + st) * 512, p.do_c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int qq = lane + 32 * u;
+        const int q = q0 + qq;
+        float l2 = 0.f, dd = 0.f;
+        if (q < p.N) {
+          l2 = p.lse[(long long)bh * p.N + q] * p.l2e;
+          dd = p.Dvec[(long long)bh * p.N + q];
+        }
+        lse2[st * BQ + qq] = l2;
+        dvec[st * BQ + qq] = dd;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        uint8_t* sb = smem + BL::STG + st * BL::STAGE_BYTES;
+        mbar_arrive_expect_tx(&in_full[st], BL::STAGE_BYTES);
+        tma_load_3d(sb + BL::Q4, &p.tm_q4, &in_full[st], 0, q0, bh);
+        tma_load_3d(sb + BL::DOR, &p.tm_do_r, &in_full[st], 0, q0, bh);
+        tma_load_3d(sb + BL::Q8, &p.tm_q8c, &in_full[st], q0, 0, bh);
+        tma_load_3d(sb + BL::DOC, &p.tm_do_c, &in_full[st], q0, 0, bh);
+      }
+      issued = t + 1;
+    }
+    if (*abort_flag && lane == 0) {
+      volatile int no_abort = 0;
+      mbar_wait(fix_full, 0, &no_abort, p.err);
+      for (int t = max(0, issued - 2); t < issued; ++t) mbar_wait(&in_full[t & 1], (t >> 1) & 1, &no_abort, p.err);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_st = idesc_bs(128, BQ, 1, 1, false, false, 0, 0);      // mxf4
+      const uint32_t id_dp = idesc_bs(128, BQ, 0, 0, false, false, 0, 0);      // mxf8 e4m3
+      const uint32_t id_acc = idesc_bs(128, D, 0, 0, false, false, 0, 0);
+      const uint32_t id_dq = idesc_bs(128, BQ, 0, 0, false, true, 0, 0);
+      const uint32_t s_k4 = smem_u32(smem + BL::K4), s_v8 = smem_u32(smem + BL::V8),
+                     s_k8 = smem_u32(smem + BL::K8), s_pq = smem_u32(smem + BL::PQ),
+                     s_dsc = smem_u32(smem + BL::DSC), s_dsr = smem_u32(smem + BL::DSR);
+      bool ok = mbar_wait(fix_full, 0, abort_flag, p.err);
+      tc_fence_after();
+      if (ok) {
+        tmem_cp_sf(tbase + SF_K4, sfc + 0 * 512);
+        tmem_cp_sf(tbase + SF_V8, sfc + 1 * 512);
+        tmem_cp_sf(tbase + SF_K8, sfc + 2 * 512);
+      }
+      for (int t = 0; ok && t < nsteps; ++t) {
+        const int st = t & 1;
+        if (!mbar_wait(&in_full[st], (t >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sb = smem_u32(smem + BL::STG + st * BL::STAGE_BYTES);
+        tmem_cp_sf(tbase + SF_Q4 + 4 * st, sfc + (6 + st) * 512);
+        tmem_cp_sf(tbase + SF_DOR + 4 * st, sfc + (8 + st) * 512);
+        tmem_cp_sf(tbase + SF_Q8 + 4 * st, sfc + (10 + st) * 512);
+        tmem_cp_sf(tbase + SF_DOC + 4 * st, sfc + (12 + st) * 512);
+        // S^T = K4 Q4^T (K = d = 128: 2 x K64)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const uint32_t sf = ((uint32_t)(2 * k) << 29) | ((uint32_t)(2 * k) << 4);
+          mma_mxf4(tbase + COL_ST, make_sdesc(s_k4 + 32 * k, 16, 512, SW_64B),
+                   make_sdesc(sb + BL::Q4 + 32 * k, 16, 512, SW_64B), id_st | sf, tbase + SF_K4,
+                   tbase + SF_Q4 + 4 * st, k > 0);
+        }
+        // dP^T = V8r dOr^T (K = d: 4 x K32)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t sf = ((uint32_t)k << 29) | ((uint32_t)k << 4);
+          mma_mxf8(tbase + COL_DPT, make_sdesc(s_v8 + 32 * k, 16, 1024, SW_128B),
+                   make_sdesc(sb + BL::DOR + 32 * k, 16, 1024, SW_128B), id_dp | sf, tbase + SF_V8,
+                   tbase + SF_DOR + 4 * st, k > 0);
+        }
+        mma_commit(s_full);
+        if (!mbar_wait(p_full, t & 1, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        tmem_cp_sf(tbase + SF_P, sfc + 3 * 512);
+        tmem_cp_sf(tbase + SF_DSC, sfc + 4 * 512);
+        tmem_cp_sf(tbase + SF_DSR, sfc + 5 * 512);
+        // dV += Pq^T dOc, dK += dSc^T Q8c (K = 64 queries: 2 x K32)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const uint32_t sf = ((uint32_t)k << 29) | ((uint32_t)k << 4);
+          mma_mxf8(tbase + COL_DV, make_sdesc(s_pq + 32 * k, 16, 512, SW_64B),
+                   make_sdesc(sb + BL::DOC + 32 * k, 16, 512, SW_64B), id_acc | sf, tbase + SF_P,
+                   tbase + SF_DOC + 4 * st, t > 0 || k > 0);
+          mma_mxf8(tbase + COL_DK, make_sdesc(s_dsc + 32 * k, 16, 512, SW_64B),
+                   make_sdesc(sb + BL::Q8 + 32 * k, 16, 512, SW_64B), id_acc | sf, tbase + SF_DSC,
+                   tbase + SF_Q8 + 4 * st, t > 0 || k > 0);
+        }
+        // dQ^T = K8c^T dSr (K = 128 keys: 4 x K32; dSr stored [keys][64 q], MN-major)
+        if (t >= 1 && !mbar_wait(dq_free, (t - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t sf = ((uint32_t)k << 29) | ((uint32_t)k << 4);
+          mma_mxf8(tbase + COL_DQT, make_sdesc(s_k8 + 32 * k, 16, 1024, SW_128B),
+                   make_sdesc(s_dsr + 2048 * k, 8192, 512, SW_64B), id_dq | sf, tbase + SF_K8,
+                   tbase + SF_DSR, k > 0);
+        }
+        mma_commit(dq_full);
+        mma_commit(&in_empty[st]);
+      }
+      mma_commit(acc_done);
+      mma_commit(mma_done);
+      volatile int no_abort = 0;
+      mbar_wait(mma_done, 0, &no_abort, p.err);
+    }
+    __syncwarp();
+  } else if (warp < 10) {
+    // ------------------------------------------------------------ P / dS
+    const int quad = warp & 3;
+    const int g = (warp - 2) >> 2;            // query group 0..1 (32 queries each)
+    const int r = quad * 32 + lane;           // key row
+    const int key = k0 + r;
+    const uint32_t lane_base = tbase + ((uint32_t)(quad * 32) << 16);
+    const float c = p.c;
+    bool ok = true;
+    uint8_t* pq = smem + BL::PQ;
+    uint8_t* dsc = smem + BL::DSC;
+    uint8_t* dsr = smem + BL::DSR;
+    for (int t = 0; t < nsteps; ++t) {
+      const int st = t & 1;
+      const int q0 = (i0 + t % per_head) * BQ;
+      if (!mbar_wait(s_full, t & 1, abort_flag, p.err)) { ok = false; break; }
+      // LSE / D of this stage were written by the producer's threads
+      if (!mbar_wait(&in_full[st], (t >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
+      tc_fence_after();
+      float s[32], dp[32];
+      {
+        uint32_t v[32];
+        tmem_ld32(lane_base + COL_ST + 32 * g, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(v[i]);
+        tmem_ld32(lane_base + COL_DPT + 32 * g, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) dp[i] = __uint_as_float(v[i]);
+      }
+      const float* l2v = lse2 + st * BQ + 32 * g;
+      const float* dv = dvec + st * BQ + 32 * g;
+      const int qbase = q0 + 32 * g;
+      float pmax = 0.f, dsmax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int q = qbase + i;
+        const bool valid = key < p.N && q < p.N && (!p.causal || key <= q);
+        const float pv = valid ? ex2_approx(fmaf(s[i], c, -l2v[i])) : 0.f;
+        const float ds = pv * (dp[i] - dv[i]);
+        s[i] = pv;
+        dp[i] = ds;
+        pmax = fmaxf(pmax, pv);
+        dsmax = fmaxf(dsmax, fabsf(ds));
+      }
+      // P and dS in blocks of 32 queries (this thread's columns)
+      float inv;
+      uint4 lo, hi;
+      const int xp = e4m3_block_exp(pmax, &inv);
+      e4m3x32(s, inv, lo, hi);
+      st_row_sw64(pq, r, g, lo, hi);
+      const int xc = e4m3_block_exp(dsmax, &inv);
+      e4m3x32(dp, inv, lo, hi);
+      st_row_sw64(dsc, r, g, lo, hi);
+      sfc[3 * 512 + lane * 16 + quad * 4 + g] = (uint8_t)(xp + 127);
+      sfc[4 * 512 + lane * 16 + quad * 4 + g] = (uint8_t)(xc + 127);
+      // dS in blocks of 32 keys (the 32 lanes of this warp) per query column
+      float q8[32];
+      uint32_t my_scale = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const uint32_t am = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(dp[i])));
+        float iv;
+        const int x = e4m3_block_exp(__uint_as_float(am), &iv);
+        q8[i] = dp[i] * iv;
+        if (lane == i) my_scale = (uint32_t)(x + 127);
+      }
+      e4m3x32(q8, 1.f, lo, hi);
+      st_row_sw64(dsr, r, g, lo, hi);
+      sfc[5 * 512 + lane * 16 + g * 4 + quad] = (uint8_t)my_scale;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    // dV, dK out
+    if (ok && mbar_wait(acc_done, 0, abort_flag, p.err)) {
+      tc_fence_after();
+      const bool valid = key < p.N;
+      const long long orow = ((long long)bkv * p.N + key) * D;
+#pragma unroll 1
+      for (int cc = 2 * g; cc < 2 * g + 2; ++cc) {    // 4 x 32 columns, 2 per group
+        uint32_t v[32];
+        tmem_ld32(lane_base + COL_DV + 32 * cc, v);
+        tmem_ld_wait();
+        if (valid) {
+          float4* dst = reinterpret_cast<float4*>(p.dv + orow + 32 * cc);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        }
+        tmem_ld32(lane_base + COL_DK + 32 * cc, v);
+        tmem_ld_wait();
+        if (valid) {
+          float4* dst = reinterpret_cast<float4*>(p.dk + orow + 32 * cc);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(v[4 * q]) * p.scale, __uint_as_float(v[4 * q + 1]) * p.scale,
+                                 __uint_as_float(v[4 * q + 2]) * p.scale, __uint_as_float(v[4 * q + 3]) * p.scale);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ writer
+    const int quad = warp & 3;
+    const int drow = quad * 32 + lane;
+    const uint32_t lane_base = tbase + ((uint32_t)(quad * 32) << 16);
+    for (int t = 0; t < nsteps; ++t) {
+      const int h = hk * group + t / per_head;
+      const int q0 = (i0 + t % per_head) * BQ;
+      if (!mbar_wait(dq_full, t & 1, abort_flag, p.err)) break;
+      tc_fence_after();
+      uint32_t v0[32], v1[32];
+      tmem_ld32(lane_base + COL_DQT, v0);
+      tmem_ld32(lane_base + COL_DQT + 32, v1);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_free);
+      float* dst = p.dq + ((long long)(b * p.Hq + h) * p.N + q0) * D + drow;
+      const int nq = min(BQ, p.N - q0);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < nq) atomicAdd(dst + (long long)i * D, __uint_as_float(v0[i]) * p.scale);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (32 + i < nq) atomicAdd(dst + (long long)(32 + i) * D, __uint_as_float(v1[i]) * p.scale);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tbase, TMEM_COLS);
+}
+
+// D_i = sum_t dO_it * O_it (one warp per row) and dq = 0.
+template <bool O_BF16>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const void* __restrict__ o,
+                                                        const __nv_bfloat16* __restrict__ dout,
+                                                        long long rows, float* __restrict__ Dvec,
+                                                        float* __restrict__ dq) {
+  const int lane = threadIdx.x % 32;
+  const long long wpb = blockDim.x / 32;
+  for (long long row = blockIdx.x * wpb + threadIdx.x / 32; row < rows; row += (long long)gridDim.x * wpb) {
+    const long long base = row * D + lane * 4;
+    const uint2 dw = *reinterpret_cast<const uint2*>(dout + base);
+    float dof[4] = {__uint_as_float(dw.x << 16), __uint_as_float(dw.x & 0xffff0000u),
+                    __uint_as_float(dw.y << 16), __uint_as_float(dw.y & 0xffff0000u)};
+    float of[4];
+    if (O_BF16) {
+      const uint2 ow = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(o) + base);
+      of[0] = __uint_as_float(ow.x << 16); of[1] = __uint_as_float(ow.x & 0xffff0000u);
+      of[2] = __uint_as_float(ow.y << 16); of[3] = __uint_as_float(ow.y & 0xffff0000u);
+    } else {
+      const float4 ov = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(o) + base);
+      of[0] = ov.x; of[1] = ov.y; of[2] = ov.z; of[3] = ov.w;
+    }
+    float acc = dof[0] * of[0] + dof[1] * of[1] + dof[2] * of[2] + dof[3] * of[3];
+#pragma unroll
+    for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) Dvec[row] = acc;
+    *reinterpret_cast<float4*>(dq + base) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_prep(const BwdPrepParams& p, cudaStream_t st) {
+  const long long rows = (long long)p.B * p.Hq * p.N;
+  cudaError_t e;
+  if ((e = launch_quantize(p.dout, rows, p.d, p.N, (long long)p.B * p.Hq, 1, 0, p.do_r, p.do_r_s, st)) != cudaSuccess) return e;
+  if ((e = launch_quantize(p.dout, rows, p.d, p.N, (long long)p.B * p.Hq, 1, 1, p.do_c, p.do_c_s, st)) != cudaSuccess) return e;
+  long long blocks = (rows + 7) / 8;
+  int grid = (int)(blocks < 152 * 16 ? blocks : 152 * 16);
+  if (p.o_bf16)
+    bwd_prep_kernel<true><<<grid, 256, 0, st>>>(p.o, (const __nv_bfloat16*)p.dout, rows, p.Dvec, p.dq);
+  else
+    bwd_prep_kernel<false><<<grid, 256, 0, st>>>(p.o, (const __nv_bfloat16*)p.dout, rows, p.Dvec, p.dq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t st) {
+  dim3 grid((p.N + BK - 1) / BK, p.B * p.Hkv);
+  cudaFuncSetAttribute(bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BL::BYTES);
+  bwd_kernel<<<grid, NTHREADS, BL::BYTES, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fa4

@@ -1,0 +1,83 @@
+"""Quantized backward on the GPU vs the oracle on the same seeded inputs.
+
+Each side runs its own forward for O (FP32) and LSE, its own MXFP4/MXFP8
+views, then the backward.  Tolerance: rel-L2 <= 1e-3 and max-abs <= 1e-2 on
+dQ, dK, dV (FP32 outputs).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_util import assert_close, require_gpu
+from precision_attention_fa4fp4_gb300.inputs import TRAIN_8B, Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_grads(fa, q, k, v, do, causal):
+    q, k, v, do = (t.cuda() for t in (q, k, v, do))
+    q4, k4 = fa.quantize(q), fa.quantize(k)
+    vt = fa.quantize(v, fa.FMT_MXFP4, fa.ALONG_N)
+    q8c = fa.quantize(q, fa.FMT_MXFP8, fa.ALONG_N)
+    k8c = fa.quantize(k, fa.FMT_MXFP8, fa.ALONG_N)
+    v8r = fa.quantize(v, fa.FMT_MXFP8, fa.ALONG_D)
+    o, lse = fa.fwd(q4, k4, vt, causal=causal, out_dtype=fa.OUT_F32)
+    dq, dk, dv = fa.bwd(q4, k4, q8c, k8c, v8r, o, do, lse, causal=causal)
+    fa.sync_status()
+    return dq.cpu().numpy(), dk.cpu().numpy(), dv.cpu().numpy()
+
+
+def oracle_views(q, k, v):
+    qf, kf, vf = (t.float().numpy() for t in (q, k, v))
+    Q4 = oracle.dequantize(*oracle.quantize(qf, 0, 0), qf.shape, 0, 0)
+    K4 = oracle.dequantize(*oracle.quantize(kf, 0, 0), kf.shape, 0, 0)
+    V4 = oracle.dequantize(*oracle.quantize(vf, 0, 1), vf.shape, 0, 1)
+    Q8 = oracle.dequantize(*oracle.quantize(qf, 1, 1), qf.shape, 1, 1)
+    K8 = oracle.dequantize(*oracle.quantize(kf, 1, 1), kf.shape, 1, 1)
+    V8 = oracle.dequantize(*oracle.quantize(vf, 1, 0), vf.shape, 1, 0)
+    return Q4, K4, V4, Q8, K8, V8
+
+
+def check(w: Workload, qrows=None, krows=None, heads_for_fwd=None, seed=0):
+    fa = require_gpu()
+    q, k, v, do = make_inputs(w, seed=seed, with_dout=True)
+    dq, dk, dv = gpu_grads(fa, q, k, v, do, w.causal)
+    Q4, K4, V4, Q8, K8, V8 = oracle_views(q, k, v)
+    if heads_for_fwd is None:
+        rows = None
+    else:
+        rows = np.concatenate([h * w.N + np.arange(w.N) for h in heads_for_fwd])
+    O, L = oracle.fwd(Q4, K4, V4, causal=w.causal, rows=rows)
+    Of = np.zeros((w.B * w.Hq * w.N, w.d), np.float32)
+    Lf = np.zeros(w.B * w.Hq * w.N, np.float32)
+    idx = np.arange(w.B * w.Hq * w.N) if rows is None else rows
+    Of[idx] = O.astype(np.float32)
+    Lf[idx] = L.astype(np.float32)
+    Of = Of.reshape(w.B, w.Hq, w.N, w.d)
+    Lf = Lf.reshape(w.B, w.Hq, w.N)
+    dQ, dK, dV = oracle.bwd(Q4, K4, Q8, K8, V8, Of, do.float().numpy(), Lf, causal=w.causal,
+                            qrows=qrows, krows=krows)
+    qsel = np.arange(w.B * w.Hq * w.N) if qrows is None else np.asarray(qrows)
+    ksel = np.arange(w.B * w.Hkv * w.N) if krows is None else np.asarray(krows)
+    assert_close(dq.reshape(-1, w.d)[qsel], dQ, w.name + " dQ")
+    assert_close(dk.reshape(-1, w.d)[ksel], dK, w.name + " dK")
+    assert_close(dv.reshape(-1, w.d)[ksel], dV, w.name + " dV")
+
+
+@pytest.mark.parametrize("N", [64, 200, 300])
+@pytest.mark.parametrize("causal", [True, False])
+def test_small(N, causal):
+    check(Workload(f"bwd_n{N}", 1, 4, 2, N, 128, causal=causal, qk_std=128 ** -0.25), seed=N)
+
+
+def test_train_causal_gqa_sampled():
+    """Causal GQA training shape: the kv head (b=1, hk=5) in full for dK/dV on
+    its first and last key tiles, dQ on two query tiles of its first head."""
+    w = TRAIN_8B
+    b, hk = 1, 5
+    heads = [b * w.Hq + hk * 4 + u for u in range(4)]
+    kbase = (b * w.Hkv + hk) * w.N
+    krows = np.concatenate([kbase + np.arange(0, 128), kbase + np.arange(w.N - 128, w.N)])
+    qbase = heads[0] * w.N
+    qrows = np.concatenate([qbase + np.arange(0, 128), qbase + np.arange(4096, 4224)])
+    check(w, qrows=qrows, krows=krows, heads_for_fwd=heads)
