@@ -128,6 +128,28 @@ FA4FP4_API fa4fp4_status fa4fp4_bwd(const void* q4_codes, const void* q4_scales,
                          float softmax_scale, int causal, float* dq, float* dk, float* dv,
                          void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the fixed device scratch array used by fa4fp4_bwd_noalloc. */
+#define FA4FP4_BWD_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* fa4fp4_bwd for callers that cannot allocate device memory (inside a graph
+ * capture that must not allocate, plugins whose host owns all allocations,
+ * runtimes that forbid allocation after start-up).  The paper has no
+ * counterpart: this is a deployment variant of fa4fp4_bwd.  Same arguments
+ * and results as fa4fp4_bwd without the workspace; the scratch is a fixed
+ * FA4FP4_BWD_NOALLOC_SCRATCH_BYTES device array inside this library (held by
+ * every GPU that loads it until exit).  Returns FA4FP4_ERR_WORKSPACE when
+ * fa4fp4_bwd_workspace_bytes(...) exceeds that size.  Allocates nothing.
+ * The first call on a device looks up the array's device address on that
+ * device; make that first call before any stream capture.  All calls share
+ * the array: calls that overlap on the GPU (other streams or host threads)
+ * race on it. */
+FA4FP4_API fa4fp4_status fa4fp4_bwd_noalloc(
+    const void* q4_codes, const void* q4_scales, const void* k4_codes, const void* k4_scales,
+    const void* q8c_codes, const void* q8c_scales, const void* k8c_codes, const void* k8c_scales,
+    const void* v8r_codes, const void* v8r_scales, const void* o, int o_dtype, const void* dout,
+    const float* lse, int B, int Hq, int Hkv, int N, int d, float softmax_scale, int causal,
+    float* dq, float* dk, float* dv, void* stream);
+
 /* BF16 FlashAttention forward, the speedup reference for fa4fp4_fwd
  * (technical summary, Results: "HAO's BF16 baseline").  q [B][Hq][N][d], k/v
  * [B][Hkv][N][d] bf16; exact online softmax with P rounded to bf16 for the

@@ -205,3 +205,33 @@ def directp_codes(s: torch.Tensor, m: float, c: float, native_exp: bool = False)
 def sync_status(device=None):
     """Synchronize the current stream and raise on a device watchdog error."""
     _check("fa4fp4_sync_status", load_library().fa4fp4_sync_status(_stream(device)))
+
+
+def bwd_noalloc(q4: QTensor, k4: QTensor, q8c: QTensor, k8c: QTensor, v8r: QTensor, o: torch.Tensor,
+                dout: torch.Tensor, lse: torch.Tensor, causal: bool = True, softmax_scale: float = 0.0,
+                dq=None, dk=None, dv=None):
+    """fa4fp4_bwd_noalloc: the backward for callers that cannot allocate device
+    memory.  The C entry point takes no workspace and allocates nothing; its
+    scratch is a fixed array inside the library (FA4FP4_BWD_NOALLOC_SCRATCH_BYTES),
+    so problems whose workspace would be larger are rejected.  Calls that
+    overlap on the GPU share that array and race.  Pass dq/dk/dv to avoid the
+    output allocations made here on the caller's behalf."""
+    lib = load_library()
+    fn = lib.fa4fp4_bwd_noalloc
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.restype = i
+    fn.argtypes = [vp] * 11 + [i, vp, vp, i, i, i, i, i, f, i, vp, vp, vp, vp]
+    B, Hq, N, d = q4.shape
+    Hkv = k4.shape[1]
+    dev = dout.device
+    dq = dq if dq is not None else torch.empty((B, Hq, N, d), dtype=torch.float32, device=dev)
+    dk = dk if dk is not None else torch.empty((B, Hkv, N, d), dtype=torch.float32, device=dev)
+    dv = dv if dv is not None else torch.empty((B, Hkv, N, d), dtype=torch.float32, device=dev)
+    o_dtype = OUT_BF16 if o.dtype == torch.bfloat16 else OUT_F32
+    _cuda(o, dout, lse, dq, dk, dv)
+    _check("fa4fp4_bwd_noalloc", fn(
+        _ptr(q4.codes), _ptr(q4.scales), _ptr(k4.codes), _ptr(k4.scales), _ptr(q8c.codes), _ptr(q8c.scales),
+        _ptr(k8c.codes), _ptr(k8c.scales), _ptr(v8r.codes), _ptr(v8r.scales), _ptr(o), o_dtype, _ptr(dout),
+        _ptr(lse), B, Hq, Hkv, N, d, float(softmax_scale), int(bool(causal)), _ptr(dq), _ptr(dk), _ptr(dv),
+        _stream(dev)))
+    return dq, dk, dv
