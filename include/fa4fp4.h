@@ -158,13 +158,13 @@ FA4FP4_API fa4fp4_status fa4bf16_fwd(const void* q, const void* k, const void* v
                           int N, int d, float softmax_scale, int causal, void* o, int out_dtype,
                           float* lse, void* stream);
 
-/* Direct-P code map on its own, with the device routines fa4fp4_fwd uses.
- * native_exp = 0: the exact threshold classifier, codes[i] = #{k :
- *   fmaf(s[i], c, -fl32(m*c)) >= T_k};
- * native_exp = 1: the native-exponential route ("selective native
- *   exponentials", Methodology 1), codes[i] = RNE_E2M1(ex2(fmaf(s[i], c,
- *   log2(6) - fl32(m*c)))); it differs from the exact map only for offsets
- *   within the hardware exp2 error of a threshold.
+/* Direct-P code map on its own, with the device routines fa4fp4_fwd uses
+ * (technical summary, Methodology 1 "Direct Mapping", which allows hardware
+ * exponentials for part of the classification).
+ * For every score: codes[i] = #{k : fmaf(s[i], c, -fl32(m*c)) >= T_k}.
+ * native_exp = 0 computes it with the threshold count; native_exp = 1 with
+ * the forward's route: e = ex2(x), codes of 6e(1-2^-18) and 6e(1+2^-18), the
+ * threshold count only where those two differ.  Both give identical codes.
  * s: n FP32 scores, codes: n bytes (device arrays). */
 FA4FP4_API fa4fp4_status fa4fp4_directp_codes(const float* s, int64_t n, float m, float c,
                                               int native_exp, uint8_t* codes, void* stream);

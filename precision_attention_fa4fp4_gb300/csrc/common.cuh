@@ -349,3 +349,20 @@ FA4_DEV uint32_t cvt_e2m1x2(float a, float b) {
 }
 
 }  // namespace fa4
+
+namespace fa4 {
+
+// 4-byte asynchronous global->shared copy; src_bytes = 0 writes zeros.
+FA4_DEV void cp_async4(void* dst_smem, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst_smem)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+// The mbarrier phase cannot complete before this thread's earlier cp.async
+// copies have landed (pending count +1 now, arrive when they complete).
+FA4_DEV void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+}  // namespace fa4

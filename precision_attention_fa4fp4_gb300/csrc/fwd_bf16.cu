@@ -5,10 +5,12 @@
 //
 // Same CTA organisation as the FP4 kernel: one CTA per (batch*head,
 // 128-query tile); warp 0 TMA producer, warp 1 TMEM owner + tcgen05.mma
-// (kind::f16, BF16 x BF16 -> FP32) issuer, warps 2-5 softmax with one query
-// row per thread.  Exact online softmax: P = 2^(c*s - c*m) (MUFU ex2), the
-// normalizer summed from FP32 P, P rounded to BF16 for the P V product, O
-// rescaled in TMEM whenever the running max grows.
+// (kind::f16, BF16 x BF16 -> FP32) issuer, warps 2-17 softmax: thread (row r,
+// column group g) owns S[r][32g, 32g+32), the row max is exchanged through
+// shared memory.  Exact online softmax: P = 2^(c*s - c*m) (MUFU ex2), the
+// normalizer summed from FP32 P (per-thread partial sums, combined at the
+// end), P rounded to BF16 for the P V product, O rescaled in TMEM whenever the
+// running max grows.
 // Q, K and P are K-major with the 128-byte swizzle (64-element chunks); V is
 // consumed MN-major straight from its row-major [keys][d] layout.
 #include <cuda_bf16.h>
@@ -19,7 +21,8 @@ namespace fa4 {
 namespace {
 
 constexpr int BM = 128, BN = 128;
-constexpr int NTHREADS = 192;
+constexpr int NSOFT = 16;
+constexpr int NTHREADS = 32 * (2 + NSOFT);
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256;
 
@@ -35,8 +38,9 @@ struct SmemB {
   static constexpr int OFF_K = OFF_Q + QB;
   static constexpr int OFF_V = OFF_K + STAGES * KB;
   static constexpr int OFF_P = OFF_V + STAGES * VB;
-  static constexpr int OFF_BAR = OFF_P + PB;
-  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 1 + 1 + 1;
+  static constexpr int OFF_RED = OFF_P + PB;                // float [2][4][128]
+  static constexpr int OFF_BAR = OFF_RED + 2 * 4 * 128 * 4;
+  static constexpr int NBAR = 1 + 4 * STAGES + 2 + 2 + 1 + 1 + 1 + 8;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int BYTES = OFF_MISC + 64 + 1024;
 };
@@ -49,15 +53,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_bf16_kernel(const __grid_cons
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = kv_full + STAGES;
-  uint64_t* s_full = kv_empty + STAGES;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + STAGES;
+  uint64_t* v_full = k_empty + STAGES;
+  uint64_t* v_empty = v_full + STAGES;
+  uint64_t* s_full = v_empty + STAGES;
   uint64_t* s_free = s_full + 2;
   uint64_t* p_full = s_free + 2;
   uint64_t* o_done = p_full + 1;
   uint64_t* mma_done = o_done + 1;
+  uint64_t* red_bar = mma_done + 1;          // [2 parities][4 quadrants]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+  float* red = reinterpret_cast<float*>(smem + L::OFF_RED);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nq = (p.N + BM - 1) / BM;
@@ -71,11 +79,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_bf16_kernel(const __grid_cons
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < STAGES; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
-    for (int s = 0; s < 2; ++s) { mbar_init(&s_full[s], 1); mbar_init(&s_free[s], 4); }
-    mbar_init(p_full, 4);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) { mbar_init(&s_full[s], 1); mbar_init(&s_free[s], NSOFT); }
+    mbar_init(p_full, NSOFT);
     mbar_init(o_done, 1);
     mbar_init(mma_done, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&red_bar[i], 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -93,21 +105,33 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_bf16_kernel(const __grid_cons
       mbar_arrive_expect_tx(q_full, L::QB);
       for (int c = 0; c < D / 64; ++c)
         tma_load_3d(smem + L::OFF_Q + c * L::CH, &p.tm_q, q_full, 64 * c, q0, bh);
-      int issued = 0;
-      for (int j = 0; j < nt; ++j) {
-        const int st = j % STAGES;
-        if (j >= STAGES && !mbar_wait(&kv_empty[st], ((j / STAGES) - 1) & 1, abort_flag, p.err)) break;
-        mbar_arrive_expect_tx(&kv_full[st], L::KB + L::VB);
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d(smem + L::OFF_K + st * L::KB + c * L::CH, &p.tm_k, &kv_full[st], 64 * c, j * BN, bkv);
-          tma_load_3d(smem + L::OFF_V + st * L::VB + c * L::CH, &p.tm_v, &kv_full[st], 64 * c, j * BN, bkv);
+      // K_j is released by QK_j, V_j only by P_j V_j: two rings, K loaded
+      // one tile ahead of V so that a slow V slot never holds back K
+      int issued_k = 0, issued_v = 0;
+      for (int j = 0; j <= nt; ++j) {
+        if (j < nt) {
+          const int st = j % STAGES;
+          if (j >= STAGES && !mbar_wait(&k_empty[st], ((j / STAGES) - 1) & 1, abort_flag, p.err)) break;
+          mbar_arrive_expect_tx(&k_full[st], L::KB);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(smem + L::OFF_K + st * L::KB + c * L::CH, &p.tm_k, &k_full[st], 64 * c, j * BN, bkv);
+          issued_k = j + 1;
         }
-        issued = j + 1;
+        if (j >= 1) {
+          const int t = j - 1, st = t % STAGES;
+          if (t >= STAGES && !mbar_wait(&v_empty[st], ((t / STAGES) - 1) & 1, abort_flag, p.err)) break;
+          mbar_arrive_expect_tx(&v_full[st], L::VB);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(smem + L::OFF_V + st * L::VB + c * L::CH, &p.tm_v, &v_full[st], 64 * c, t * BN, bkv);
+          issued_v = t + 1;
+        }
       }
       if (*abort_flag) {
         volatile int no_abort = 0;
-        for (int j = max(0, issued - STAGES); j < issued; ++j)
-          mbar_wait(&kv_full[j % STAGES], (j / STAGES) & 1, &no_abort, p.err);
+        for (int j = max(0, issued_k - STAGES); j < issued_k; ++j)
+          mbar_wait(&k_full[j % STAGES], (j / STAGES) & 1, &no_abort, p.err);
+        for (int j = max(0, issued_v - STAGES); j < issued_v; ++j)
+          mbar_wait(&v_full[j % STAGES], (j / STAGES) & 1, &no_abort, p.err);
       }
     }
     __syncwarp();
@@ -120,9 +144,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_bf16_kernel(const __grid_cons
       bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
       tc_fence_after();
       auto issue_pv = [&](int t) -> bool {
+        const int st = t % STAGES;
+        if (!mbar_wait(&v_full[st], (t / STAGES) & 1, abort_flag, p.err)) return false;
         if (!mbar_wait(p_full, t & 1, abort_flag, p.err)) return false;
         tc_fence_after();
-        const int st = t % STAGES;
         const uint32_t sv = smem_u32(smem + L::OFF_V + st * L::VB);
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
@@ -131,12 +156,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_bf16_kernel(const __grid_cons
           mma_f16(tbase + COL_O, ad, bd, idesc_o, t > 0 || k > 0);
         }
         mma_commit(o_done);
-        mma_commit(&kv_empty[st]);
+        mma_commit(&v_empty[st]);
         return true;
       };
       for (int j = 0; ok && j < nt; ++j) {
         const int st = j % STAGES;
-        if (!mbar_wait(&kv_full[st], (j / STAGES) & 1, abort_flag, p.err)) { ok = false; break; }
+        if (!mbar_wait(&k_full[st], (j / STAGES) & 1, abort_flag, p.err)) { ok = false; break; }
         const int sb = j & 1;
         if (j >= 2 && !mbar_wait(&s_free[sb], ((j >> 1) - 1) & 1, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
@@ -148,6 +173,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_bf16_kernel(const __grid_cons
                   make_sdesc(sk + off, 16, 1024, SW_128B), idesc_s, k > 0);
         }
         mma_commit(&s_full[sb]);
+        mma_commit(&k_empty[st]);
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
       if (ok && nt > 0) issue_pv(nt - 1);
@@ -158,47 +184,55 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_bf16_kernel(const __grid_cons
     __syncwarp();
   } else {
     const int quad = warp & 3;
+    const int g = (warp - 2) >> 2;            // column group 0..3
     const int r = quad * 32 + lane;
     const int qi = q0 + r;
     const uint32_t lane_base = tbase + ((uint32_t)(quad * 32) << 16);
     const float c = p.c;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;             // l: this thread's partial sum
     bool ok = true;
+    // P row r: keys 64*(g/2) .. in chunk g/2; this thread's 4 16-byte pieces
+    uint8_t* prow = smem + L::OFF_P + (g >> 1) * L::CH + r * 128;
     for (int j = 0; j < nt; ++j) {
       const int sb = j & 1;
       if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
       tc_fence_after();
-      float s[BN];
-#pragma unroll
-      for (int cc = 0; cc < BN / 32; ++cc) {
+      float s[32];
+      {
         uint32_t v[32];
-        tmem_ld32(lane_base + (sb ? COL_S1 : COL_S0) + cc * 32, v);
+        tmem_ld32(lane_base + (sb ? COL_S1 : COL_S0) + 32 * g, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(v[i]);
+        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(v[i]);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[sb]);
-      const int kbase = j * BN;
-      if (kbase + BN > p.N || (p.causal && kbase + BN - 1 > q0)) {
+      const int kbase = j * BN + 32 * g;
+      if (j * BN + BN > p.N || (p.causal && j * BN + BN - 1 > q0)) {
         const int lim = p.causal ? min(p.N - 1, qi) : p.N - 1;
 #pragma unroll
-        for (int i = 0; i < BN; ++i)
+        for (int i = 0; i < 32; ++i)
           if (kbase + i > lim) s[i] = -INFINITY;
       }
-      float tmax = s[0];
+      float pm = fmax3(s[0], s[1], s[2]);
 #pragma unroll
-      for (int i = 1; i + 1 < BN; i += 2) tmax = fmax3(tmax, s[i], s[i + 1]);
-      tmax = fmaxf(tmax, s[BN - 1]);
+      for (int i = 3; i + 1 < 32; i += 2) pm = fmax3(pm, s[i], s[i + 1]);
+      pm = fmaxf(pm, s[31]);
+      float* rslot = red + (sb * 4) * 128;
+      rslot[g * 128 + r] = pm;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&red_bar[sb * 4 + quad]);
+      if (!mbar_wait(&red_bar[sb * 4 + quad], (j >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
+      const float tmax = fmaxf(fmaxf(rslot[r], rslot[128 + r]), fmaxf(rslot[256 + r], rslot[384 + r]));
       const float m_new = fmaxf(m, tmax);
       const float mc = m_new * c;
-      uint32_t pk[BN / 2];
+      uint32_t pk[16];
       float lsum = 0.f;
 #pragma unroll
-      for (int i = 0; i < BN / 2; ++i) {
-        float p0 = ex2_approx(fmaf(s[2 * i], c, -mc));
-        float p1 = ex2_approx(fmaf(s[2 * i + 1], c, -mc));
+      for (int i = 0; i < 16; ++i) {
+        const float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), make_float2(c, c), make_float2(-mc, -mc));
+        const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
         lsum += p0 + p1;
         __nv_bfloat162 t = __floats2bfloat162_rn(p0, p1);
         pk[i] = *reinterpret_cast<uint32_t*>(&t);
@@ -207,27 +241,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_bf16_kernel(const __grid_cons
       if (j > 0) {
         if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t v[32];
-            tmem_ld32(lane_base + COL_O + cc * 32, v);
-            tmem_ld_wait();
+        if (__any_sync(0xffffffffu, alpha != 1.f) && 32 * g < D) {
+          uint32_t v[32];
+          tmem_ld32(lane_base + COL_O + 32 * g, v);
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st32(lane_base + COL_O + cc * 32, v);
+          for (int i = 0; i < 32; i += 2) {
+            float2 t = fmul2(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                             make_float2(alpha, alpha));
+            v[i] = __float_as_uint(t.x);
+            v[i + 1] = __float_as_uint(t.y);
           }
+          tmem_st32(lane_base + COL_O + 32 * g, v);
           tmem_st_wait();
         }
       }
       l = alpha * l + lsum;
       m = m_new;
-      // P row r: keys 0-63 in chunk 0, 64-127 in chunk 1; 128-byte swizzle
-      uint8_t* prow = smem + L::OFF_P + r * 128;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const int ch = k / 8, sub = k % 8;
-        *reinterpret_cast<uint4*>(prow + ch * L::CH + ((sub ^ (r & 7)) << 4)) =
+      for (int k = 0; k < 4; ++k) {
+        const int sub = (g & 1) * 4 + k;
+        *reinterpret_cast<uint4*>(prow + ((sub ^ (r & 7)) << 4)) =
             make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
       }
       fence_proxy_async_smem();
@@ -235,19 +269,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_bf16_kernel(const __grid_cons
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
+    // combine the four partial normalizers of each row (all used the same m)
+    const int pe = nt & 1;                    // slot parity not used by the last tile
+    float* lslot = red + (pe * 4) * 128;
+    if (ok) {
+      lslot[g * 128 + r] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&red_bar[pe * 4 + quad]);
+      ok = mbar_wait(&red_bar[pe * 4 + quad], (nt >> 1) & 1, abort_flag, p.err);
+    }
     if (ok && nt > 0 && mbar_wait(o_done, (nt - 1) & 1, abort_flag, p.err)) {
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float lt = (lslot[r] + lslot[128 + r]) + (lslot[256 + r] + lslot[384 + r]);
+      const float inv_l = 1.f / lt;
       const bool valid = qi < p.N;
-      const long long orow = ((long long)bh * p.N + qi) * D;
-#pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
+      const long long orow = ((long long)bh * p.N + qi) * D + 32 * g;
+      if (32 * g < D) {
         uint32_t v[32];
-        tmem_ld32(lane_base + COL_O + cc * 32, v);
+        tmem_ld32(lane_base + COL_O + 32 * g, v);
         tmem_ld_wait();
         if (valid) {
           if (p.out_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow + cc * 32);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint32_t w[4];
@@ -260,7 +303,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_bf16_kernel(const __grid_cons
               dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
             }
           } else {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + orow + cc * 32);
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + orow);
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv_l, __uint_as_float(v[4 * q + 1]) * inv_l,
@@ -268,7 +311,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_bf16_kernel(const __grid_cons
           }
         }
       }
-      if (valid && p.lse) p.lse[(long long)bh * p.N + qi] = p.scale * m + logf(l);
+      if (g == 0 && valid && p.lse) p.lse[(long long)bh * p.N + qi] = p.scale * m + logf(lt);
     }
   }
   tc_fence_before();

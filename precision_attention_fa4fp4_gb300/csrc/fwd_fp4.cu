@@ -3,10 +3,10 @@
 // "Hardware-Aware FP4 FlashAttention-4" (arXiv:2609.04105), technical
 // summary, Methodology 1: S = Q K^T on FP4 tensor cores; each score's offset
 // from the running row max classified straight into an E2M1 probability code
-// ("Direct Mapping", by threshold comparison "or selective native
-// exponentials"); the normalizer accumulated from the same codes the P V
-// product consumes ("Consistent Normalization"); MXFP4 for P and V ("Format
-// Selection").  Q and K are MXFP4 as well.
+// (Direct Mapping: a classifier, with hardware exponentials allowed for part
+// of the work); the normalizer accumulated from the same codes the P V
+// product consumes (Consistent Normalization); MXFP4 for P and V (Format
+// Selection).  Q and K are MXFP4 as well.
 //
 // One CTA per (batch*head, 128-query tile), 18 warps:
 //   warp 0      producer: TMA loads of Q, K_j, V^T_j codes into swizzled shared
@@ -19,18 +19,14 @@
 //               the tensor core from exactly the codes P V consumes).
 //   warps 2-17  softmax: 4 warps per TMEM lane quadrant; thread (row r, column
 //               group g) owns S[r][32g, 32g+32).  Row max exchanged through
-//               shared memory (one mbarrier per quadrant), Direct-P codes,
-//               eager O rescale of its 32 O columns, one 16-byte P chunk.
+//               shared memory (one mbarrier per quadrant), Direct-P codes
+//               (native exponentials bracketed to the exact threshold map,
+//               threshold count where the bracket is ambiguous), eager O
+//               rescale of its 32 O columns, one 16-byte P chunk.
 // QK^T of tile j+1 runs on the tensor core while tile j's codes are built.
 #include <cuda_bf16.h>
 #include "common.cuh"
 #include "internal.h"
-
-// Columns of each thread's 32 that take the native-exponential route
-// (ex2 + RNE to E2M1); the rest take the exact threshold classifier.
-#ifndef FA4_NATIVE_PER_32
-#define FA4_NATIVE_PER_32 24
-#endif
 
 namespace fa4 {
 namespace {
@@ -44,7 +40,6 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_L = 384, COL_SFQ = 400,
                    COL_SFP = 404, COL_SFK = 408, COL_SFV = 408 + 4 * STAGES;
 static_assert(COL_SFV + 4 * STAGES <= TMEM_COLS, "TMEM budget");
-constexpr float LOG2_6 = 2.5849625007211562f;
 
 template <int D>
 struct Smem {
@@ -63,7 +58,7 @@ struct Smem {
                        SF_V = SF_K + 512 * STAGES;
   static constexpr int OFF_RED = SF_V + 512 * STAGES;     // float [2][4][128]
   static constexpr int OFF_BAR = OFF_RED + 2 * 4 * 128 * 4;
-  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 1 + 1 + 1 + 8;
+  static constexpr int NBAR = 1 + 4 * STAGES + 2 + 2 + 1 + 1 + 1 + 8;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int BYTES = OFF_MISC + 64 + 1024;    // + alignment slack
 };
@@ -76,25 +71,44 @@ FA4_DEV uint32_t directp_code(float x, const float (&T)[7]) {
   return c;
 }
 
-// Codes of 8 consecutive scores, packed (element e in nibble e).
-// native: RNE_E2M1(2^(x + log2 6)) via MUFU ex2; exact: threshold count.
-template <bool NATIVE>
-FA4_DEV uint32_t codes8(const float* s, float c, float mc, float bias, const float (&T)[7]) {
-  uint32_t w = 0;
-  if (NATIVE) {
+// Codes of 32 consecutive scores, packed 8 per word (element e of word w in
+// nibble e).  Native-exponential route made exact: with x = fmaf(s, c, -mc)
+// (the method's offset) and e = ex2(x), the codes of 6e(1-eps) and 6e(1+eps)
+// bracket the code of the exact 6*2^x, because rounding to E2M1 is monotone
+// and eps = 2^-18 exceeds the error of ex2 plus the two products.  Where the
+// bracket is one code wide that code is the exact one; the lanes where it is
+// not (scores within eps of an E2M1 midpoint) redo their scores with the
+// threshold count.  Returns the packed codes in pw.
+constexpr float K_LO = 6.0f * (1.0f - 0x1p-18f), K_HI = 6.0f * (1.0f + 0x1p-18f);
+
+FA4_DEV void directp_codes32(const float (&s)[32], float c, float mc, const float (&T)[7],
+                             uint32_t (&pw)[4]) {
+  bool ambiguous = false;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t lo = 0, hi = 0;
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
-      float2 x = ffma2(make_float2(s[e], s[e + 1]), make_float2(c, c), make_float2(bias, bias));
-      w |= cvt_e2m1x2(ex2_approx(x.x), ex2_approx(x.y)) << (4 * e);
+      const float2 x = ffma2(make_float2(s[8 * w + e], s[8 * w + e + 1]), make_float2(c, c),
+                             make_float2(-mc, -mc));
+      const float2 ex = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+      const float2 ylo = fmul2(ex, make_float2(K_LO, K_LO));
+      const float2 yhi = fmul2(ex, make_float2(K_HI, K_HI));
+      lo |= cvt_e2m1x2(ylo.x, ylo.y) << (4 * e);
+      hi |= cvt_e2m1x2(yhi.x, yhi.y) << (4 * e);
     }
-  } else {
+    pw[w] = lo;
+    ambiguous |= lo != hi;
+  }
+  if (__any_sync(0xffffffffu, ambiguous) && ambiguous) {
 #pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      float2 x = ffma2(make_float2(s[e], s[e + 1]), make_float2(c, c), make_float2(-mc, -mc));
-      w |= (directp_code(x.x, T) | (directp_code(x.y, T) << 4)) << (4 * e);
+    for (int w = 0; w < 4; ++w) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) word |= directp_code(fmaf(s[8 * w + e], c, -mc), T) << (4 * e);
+      pw[w] = word;
     }
   }
-  return w;
 }
 
 // Rearrange 128 rows of per-row scale words into the scale-factor chunk:
@@ -123,9 +137,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = kv_full + STAGES;
-  uint64_t* s_full = kv_empty + STAGES;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + STAGES;
+  uint64_t* v_full = k_empty + STAGES;
+  uint64_t* v_empty = v_full + STAGES;
+  uint64_t* s_full = v_empty + STAGES;
   uint64_t* s_free = s_full + 2;
   uint64_t* p_full = s_free + 2;
   uint64_t* o_done = p_full + 1;
@@ -147,12 +163,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < STAGES; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1);
+    }
     for (int s = 0; s < 2; ++s) { mbar_init(&s_full[s], 1); mbar_init(&s_free[s], NSOFT); }
     mbar_init(p_full, NSOFT);
     mbar_init(o_done, 1);
     mbar_init(mma_done, 1);
-    for (int i = 0; i < 8; ++i) mbar_init(&red_bar[i], 128);
+    for (int i = 0; i < 8; ++i) mbar_init(&red_bar[i], 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -190,30 +209,51 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
     int issued = 0;
     for (int j = 0; j < nt; ++j) {
       const int st = j % STAGES;
-      if (j >= STAGES && !mbar_wait(&kv_empty[st], ((j / STAGES) - 1) & 1, abort_flag, p.err)) break;
-      stage_sf_rows(smem + L::SF_K + 512 * st, ks, j * BN, min(BN, p.N - j * BN), D / 32, lane);
-      {
-        uint32_t w[4];
+      const int ph = ((j / STAGES) - 1) & 1;
+      // K_j: codes by TMA, scales rearranged into the chunk (cp.async for
+      // 4-byte scale words, plain loads for the 2-byte words of d = 64)
+      if (j >= STAGES && !mbar_wait(&k_empty[st], ph, abort_flag, p.err)) break;
+      uint8_t* kchunk = smem + L::SF_K + 512 * st;
+      if (D == 128) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          int ch = lane + 32 * c;
-          w[c] = ch < D ? *reinterpret_cast<const uint32_t*>(vs + (long long)ch * (p.Np / 32) + 4 * j) : 0u;
+          const int r = lane + 32 * c;
+          const bool in = j * BN + r < p.N;
+          cp_async4(kchunk + lane * 16 + 4 * c, ks + (long long)(j * BN + (in ? r : 0)) * 4, in ? 4u : 0u);
         }
-        *reinterpret_cast<uint4*>(smem + L::SF_V + 512 * st + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        cp_async_mbar_arrive(&k_full[st]);
+      } else {
+        stage_sf_rows(kchunk, ks, j * BN, min(BN, p.N - j * BN), D / 32, lane);
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(&kv_full[st], L::KB + L::VB);
-        tma_load_3d(smem + L::OFF_K + st * L::KB, &p.tm_k, &kv_full[st], 0, j * BN, bkv);
-        tma_load_3d(smem + L::OFF_V + st * L::VB, &p.tm_v, &kv_full[st], j * (BN / 2), 0, bkv);
+        mbar_arrive_expect_tx(&k_full[st], L::KB);
+        tma_load_3d(smem + L::OFF_K + st * L::KB, &p.tm_k, &k_full[st], 0, j * BN, bkv);
+      }
+      // V^T_j: channel rows, the 4 key blocks of tile j
+      if (j >= STAGES && !mbar_wait(&v_empty[st], ph, abort_flag, p.err)) break;
+      uint8_t* vchunk = smem + L::SF_V + 512 * st;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int ch = lane + 32 * c;
+        const bool in = ch < D;
+        cp_async4(vchunk + lane * 16 + 4 * c, vs + (long long)(in ? ch : 0) * (p.Np / 32) + 4 * j, in ? 4u : 0u);
+      }
+      cp_async_mbar_arrive(&v_full[st]);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&v_full[st], L::VB);
+        tma_load_3d(smem + L::OFF_V + st * L::VB, &p.tm_v, &v_full[st], j * (BN / 2), 0, bkv);
       }
       issued = j + 1;
     }
     if (*abort_flag && lane == 0) {
       volatile int no_abort = 0;
-      for (int j = max(0, issued - STAGES); j < issued; ++j)
-        mbar_wait(&kv_full[j % STAGES], (j / STAGES) & 1, &no_abort, p.err);
+      for (int j = max(0, issued - STAGES); j < issued; ++j) {
+        mbar_wait(&k_full[j % STAGES], (j / STAGES) & 1, &no_abort, p.err);
+        mbar_wait(&v_full[j % STAGES], (j / STAGES) & 1, &no_abort, p.err);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -233,9 +273,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
         tmem_cp_sf(tbase + COL_SFP, smem + L::SF_P);
       }
       auto issue_pv = [&](int t) -> bool {
+        const int st = t % STAGES;
+        if (!mbar_wait(&v_full[st], (t / STAGES) & 1, abort_flag, p.err)) return false;
+        fence_proxy_async_smem();
+        tmem_cp_sf(tbase + COL_SFV + 4 * st, smem + L::SF_V + 512 * st);
         if (!mbar_wait(p_full, t & 1, abort_flag, p.err)) return false;
         tc_fence_after();
-        const int st = t % STAGES;
         const uint32_t sp = smem_u32(smem + L::OFF_P + (t & 1) * L::PB);
         const uint32_t sv = smem_u32(smem + L::OFF_V + st * L::VB);
 #pragma unroll
@@ -248,15 +291,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
                    tbase + COL_SFP, tbase + COL_SFP, t > 0 || k > 0);
         }
         mma_commit(o_done);
-        mma_commit(&kv_empty[st]);
+        mma_commit(&v_empty[st]);
         return true;
       };
       for (int j = 0; ok && j < nt; ++j) {
         const int st = j % STAGES;
-        if (!mbar_wait(&kv_full[st], (j / STAGES) & 1, abort_flag, p.err)) { ok = false; break; }
+        if (!mbar_wait(&k_full[st], (j / STAGES) & 1, abort_flag, p.err)) { ok = false; break; }
+        fence_proxy_async_smem();
         tc_fence_after();
         tmem_cp_sf(tbase + COL_SFK + 4 * st, smem + L::SF_K + 512 * st);
-        tmem_cp_sf(tbase + COL_SFV + 4 * st, smem + L::SF_V + 512 * st);
         const int sb = j & 1;
         if (j >= 2 && !mbar_wait(&s_free[sb], ((j >> 1) - 1) & 1, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
@@ -269,6 +312,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
           mma_mxf4(tbase + (sb ? COL_S1 : COL_S0), ad, bd, id, tbase + COL_SFQ, tbase + COL_SFK + 4 * st, k > 0);
         }
         mma_commit(&s_full[sb]);
+        mma_commit(&k_empty[st]);
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
       if (ok && nt > 0) issue_pv(nt - 1);
@@ -320,18 +364,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       pm = fmaxf(pm, s[31]);
       float* rslot = red + (sb * 4) * 128;
       rslot[g * 128 + r] = pm;
-      mbar_arrive(&red_bar[sb * 4 + quad]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&red_bar[sb * 4 + quad]);
       if (!mbar_wait(&red_bar[sb * 4 + quad], (j >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
       const float tmax = fmaxf(fmaxf(rslot[r], rslot[128 + r]), fmaxf(rslot[256 + r], rslot[384 + r]));
       const float m_new = fmaxf(m, tmax);
       const float mc = m_new * c;
-      const float bias = LOG2_6 - mc;
       uint32_t pw[4];
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        if (w * 8 < FA4_NATIVE_PER_32) pw[w] = codes8<true>(s + 8 * w, c, mc, bias, T);
-        else pw[w] = codes8<false>(s + 8 * w, c, mc, bias, T);
-      }
+      directp_codes32(s, c, mc, T, pw);
       const float alpha = (m == -INFINITY) ? 1.f : ex2_approx(fmaf(m, c, -mc));
       if (j > 0) {
         if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, p.err)) { ok = false; break; }
@@ -407,6 +447,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
   if (warp == 1) tmem_dealloc(tbase, TMEM_COLS);
 }
 
+// Elementwise Direct-P codes with the forward's routines: NATIVE = the
+// bracketed native-exponential classifier (32 scores per thread), else the
+// threshold count.
 template <bool NATIVE>
 __global__ void directp_codes_kernel(const float* __restrict__ s, long long n, float m, float c,
                                      Thresh T, uint8_t* __restrict__ out) {
@@ -414,13 +457,36 @@ __global__ void directp_codes_kernel(const float* __restrict__ s, long long n, f
 #pragma unroll
   for (int k = 0; k < 7; ++k) t[k] = T.v[k];
   const float mc = m * c;
-  const float bias = LOG2_6 - mc;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x) {
-    uint32_t code;
-    if (NATIVE) code = cvt_e2m1x2(ex2_approx(fmaf(s[i], c, bias)), 0.f) & 0xfu;
-    else code = directp_code(fmaf(s[i], c, -mc), t);
-    out[i] = (uint8_t)code;
+  const long long nchunks = (n + 31) / 32;
+  for (long long ch = blockIdx.x * (long long)blockDim.x + threadIdx.x; ch - threadIdx.x < nchunks;
+       ch += (long long)gridDim.x * blockDim.x) {
+    // whole warps stay converged for the warp vote inside the classifier
+    const bool live = ch < nchunks;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const long long idx = ch * 32 + i;
+      v[i] = (live && idx < n) ? s[idx] : -INFINITY;
+    }
+    uint32_t pw[4];
+    if (NATIVE) {
+      directp_codes32(v, c, mc, t, pw);
+    } else {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) word |= directp_code(fmaf(v[8 * w + e], c, -mc), t) << (4 * e);
+        pw[w] = word;
+      }
+    }
+    if (live) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const long long idx = ch * 32 + i;
+        if (idx < n) out[idx] = (uint8_t)((pw[i / 8] >> (4 * (i % 8))) & 0xfu);
+      }
+    }
   }
 }
 
@@ -445,7 +511,7 @@ cudaError_t launch_directp_codes(const float* s, long long n, float m, float c, 
                                  int native, uint8_t* codes, cudaStream_t st) {
   Thresh t;
   for (int k = 0; k < 7; ++k) t.v[k] = T[k];
-  long long blocks = (n + 255) / 256;
+  long long blocks = ((n + 31) / 32 + 255) / 256;
   int grid = (int)(blocks < 152 * 16 ? (blocks > 0 ? blocks : 1) : 152 * 16);
   if (native) directp_codes_kernel<true><<<grid, 256, 0, st>>>(s, n, m, c, t, codes);
   else directp_codes_kernel<false><<<grid, 256, 0, st>>>(s, n, m, c, t, codes);
