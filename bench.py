@@ -94,7 +94,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
 
@@ -193,11 +193,12 @@ def run_ours(args, rank, world, local):
     def step_fwd_only(ie):
         fa.fwd(q4, k4, vt, causal=False, out_dtype=fa.OUT_BF16, out=o, lse=lse)
 
+    # clocks are sampled across every timed loop below (main step, kernel-only,
+    # BF16, end to end, training shape)
     clocks = ClockSampler(local) if rank == 0 else None
     t0 = time.time()
     step_ms, fwd_ms = time_steps(step, args.warmup, args.steps, flush, world, inner=True)
     wall = time.time() - t0
-    clock_info = clocks.stop() if clocks else None
     fa.sync_status()
     flops = w.fwd_flops
     ms = max_over_ranks(statistics.mean(step_ms), world)
@@ -238,6 +239,8 @@ def run_ours(args, rank, world, local):
         train = run_train(fa, dev, args, world)
     except Exception as e:  # reported, not hidden
         train = {"error": f"{type(e).__name__}: {e}"}
+
+    clock_info = clocks.stop() if clocks else None
 
     pk = peaks()
     fp4_peak = pk["bf16"] * FP4_OVER_BF16

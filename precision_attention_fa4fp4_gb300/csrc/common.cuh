@@ -366,3 +366,16 @@ FA4_DEV void cp_async_mbar_arrive(uint64_t* bar) {
 }
 
 }  // namespace fa4
+
+namespace fa4 {
+
+FA4_DEV float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+}  // namespace fa4

@@ -228,15 +228,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_bf16_kernel(const __grid_cons
       const float m_new = fmaxf(m, tmax);
       const float mc = m_new * c;
       uint32_t pk[16];
-      float lsum = 0.f;
+      float2 ls2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), make_float2(c, c), make_float2(-mc, -mc));
-        const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-        lsum += p0 + p1;
-        __nv_bfloat162 t = __floats2bfloat162_rn(p0, p1);
+        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        ls2 = fadd2(ls2, pp);
+        __nv_bfloat162 t = __floats2bfloat162_rn(pp.x, pp.y);
         pk[i] = *reinterpret_cast<uint32_t*>(&t);
       }
+      const float lsum = ls2.x + ls2.y;
       const float alpha = (m == -INFINITY) ? 1.f : ex2_approx(fmaf(m, c, -mc));
       if (j > 0) {
         if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, p.err)) { ok = false; break; }

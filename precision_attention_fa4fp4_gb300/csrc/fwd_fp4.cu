@@ -86,17 +86,19 @@ FA4_DEV void directp_codes32(const float (&s)[32], float c, float mc, const floa
   bool ambiguous = false;
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    uint32_t lo = 0, hi = 0;
+    float ylo[8], yhi[8];
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
       const float2 x = ffma2(make_float2(s[8 * w + e], s[8 * w + e + 1]), make_float2(c, c),
                              make_float2(-mc, -mc));
       const float2 ex = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-      const float2 ylo = fmul2(ex, make_float2(K_LO, K_LO));
-      const float2 yhi = fmul2(ex, make_float2(K_HI, K_HI));
-      lo |= cvt_e2m1x2(ylo.x, ylo.y) << (4 * e);
-      hi |= cvt_e2m1x2(yhi.x, yhi.y) << (4 * e);
+      const float2 a = fmul2(ex, make_float2(K_LO, K_LO));
+      const float2 b = fmul2(ex, make_float2(K_HI, K_HI));
+      ylo[e] = a.x; ylo[e + 1] = a.y;
+      yhi[e] = b.x; yhi[e + 1] = b.y;
     }
+    const uint32_t lo = pack_e2m1x8(ylo[0], ylo[1], ylo[2], ylo[3], ylo[4], ylo[5], ylo[6], ylo[7]);
+    const uint32_t hi = pack_e2m1x8(yhi[0], yhi[1], yhi[2], yhi[3], yhi[4], yhi[5], yhi[6], yhi[7]);
     pw[w] = lo;
     ambiguous |= lo != hi;
   }
