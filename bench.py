@@ -30,7 +30,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from precision_attention_fa4fp4_gb300.inputs import FWD_4K, TRAIN_8B, make_inputs  # noqa: E402
+from precision_attention_fa4fp4_gb300.inputs import FWD_4K, SWEEP, TRAIN_8B, VIDEO_DIT, make_inputs  # noqa: E402
 
 METRIC = "FP4 attention fwd TFLOP/s (noncausal, d=128) and speedup vs own BF16 kernel"
 FP4_OVER_BF16 = 13.5 / 2.25     # nominal dense FP4 : BF16 tensor rate on GB300
@@ -240,6 +240,12 @@ def run_ours(args, rank, world, local):
     except Exception as e:  # reported, not hidden
         train = {"error": f"{type(e).__name__}: {e}"}
 
+    workloads = None
+    if not args.no_sweep:
+        try:
+            workloads = run_workloads(fa, dev, 3)
+        except Exception as e:
+            workloads = {"error": f"{type(e).__name__}: {e}"}
     clock_info = clocks.stop() if clocks else None
 
     pk = peaks()
@@ -277,8 +283,31 @@ def run_ours(args, rank, world, local):
         "timed_wall_s": round(wall, 3),
         "clocks": clock_info,
         "train": train,
+        "workloads": workloads,
     }
     return result
+
+
+def run_workloads(fa, dev, steps):
+    """Kernel-only FP4 and BF16 forward TFLOP/s on the sweep and video-DiT
+    workloads (inputs quantized beforehand, L2 flushed before every launch)."""
+    flush = Flusher(dev)
+    out = []
+    for w in (VIDEO_DIT,) + SWEEP:
+        q, k, v = (t.to(dev) for t in make_inputs(w, seed=0))
+        q4, k4 = fa.quantize(q), fa.quantize(k)
+        vt = fa.quantize(v, fa.FMT_MXFP4, fa.ALONG_N)
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        f_ms, _ = time_steps(lambda ie: fa.fwd(q4, k4, vt, out=o, lse=lse), 2, steps, flush, 1)
+        b_ms, _ = time_steps(lambda ie: fa.bf16_fwd(q, k, v, out=o, lse=lse), 2, steps, flush, 1)
+        fa.sync_status()
+        fm, bm = statistics.mean(f_ms), statistics.mean(b_ms)
+        out.append({"workload": w.name, "fp4_tflops": round(w.fwd_flops / (fm * 1e-3) / 1e12, 1),
+                    "bf16_tflops": round(w.fwd_flops / (bm * 1e-3) / 1e12, 1), "speedup": round(bm / fm, 3)})
+        del q, k, v, q4, k4, vt, o, lse
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_train(fa, dev, args, world):
@@ -381,6 +410,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the per-workload kernel table")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":

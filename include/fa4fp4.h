@@ -169,6 +169,13 @@ FA4FP4_API fa4fp4_status fa4bf16_fwd(const void* q, const void* k, const void* v
 FA4FP4_API fa4fp4_status fa4fp4_directp_codes(const float* s, int64_t n, float m, float c,
                                               int native_exp, uint8_t* codes, void* stream);
 
+/* Watchdog self-test: launches one CTA whose pipeline wait can never be
+ * satisfied, bounded by limit_ns (0 < limit_ns <= 2e9).  The wait expires,
+ * the kernel returns, and the next fa4fp4_sync_status reports
+ * FA4FP4_ERR_DEVICE_TIMEOUT; the context stays usable.  Exercises the same
+ * bounded-wait routine every kernel of the library uses (2 s limit). */
+FA4FP4_API fa4fp4_status fa4fp4_watchdog_selftest(int64_t limit_ns, void* stream);
+
 /* Synchronizes `stream`, then returns FA4FP4_ERR_CUDA for a pending CUDA error
  * or FA4FP4_ERR_DEVICE_TIMEOUT if any kernel's bounded wait expired since the
  * last call (the flag is cleared), else FA4FP4_OK. */

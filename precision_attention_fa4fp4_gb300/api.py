@@ -202,6 +202,16 @@ def directp_codes(s: torch.Tensor, m: float, c: float, native_exp: bool = False)
     return out
 
 
+def watchdog_selftest(limit_ns: int = 50_000_000, device=None):
+    """Launch the library's watchdog self-test (a bounded wait that nothing
+    satisfies); the next sync_status() raises with FA4FP4_ERR_DEVICE_TIMEOUT."""
+    lib = load_library()
+    fn = lib.fa4fp4_watchdog_selftest
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_int64, ctypes.c_void_p]
+    _check("fa4fp4_watchdog_selftest", fn(int(limit_ns), _stream(device)))
+
+
 def sync_status(device=None):
     """Synchronize the current stream and raise on a device watchdog error."""
     _check("fa4fp4_sync_status", load_library().fa4fp4_sync_status(_stream(device)))

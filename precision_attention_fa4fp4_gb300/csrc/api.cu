@@ -297,6 +297,14 @@ fa4fp4_status fa4bf16_fwd(const void* q, const void* k, const void* v, int B, in
   return launch_status(launch_fwd_bf16(p, static_cast<cudaStream_t>(stream)));
 }
 
+fa4fp4_status fa4fp4_watchdog_selftest(int64_t limit_ns, void* stream) {
+  if (limit_ns <= 0 || limit_ns > 2000000000LL) return FA4FP4_ERR_INVALID_ARG;
+  unsigned* w = err_word();
+  if (!w) return FA4FP4_ERR_CUDA;
+  return launch_status(launch_watchdog_selftest(w, (unsigned long long)limit_ns,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 fa4fp4_status fa4fp4_sync_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return FA4FP4_ERR_CUDA;

@@ -76,10 +76,10 @@ FA4_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns false
-// (after flagging the error and the CTA abort word) on timeout or when another
-// role of the CTA already aborted.
-FA4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                       unsigned* err) {
+// (after flagging the error and the CTA abort word) once limit_ns have passed,
+// or when another role of the CTA already aborted.
+FA4_DEV bool mbar_wait_ns(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                          unsigned* err, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer();
   while (true) {
@@ -87,12 +87,17 @@ FA4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer() - t0 > FA4_WAIT_NS) {
+    if (globaltimer() - t0 > limit_ns) {
       *abort_flag = 1;
       atomicOr(err, FA4_DEVERR_TIMEOUT);
       return false;
     }
   }
+}
+
+FA4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                       unsigned* err) {
+  return mbar_wait_ns(bar, parity, abort_flag, err, FA4_WAIT_NS);
 }
 
 // ----------------------------------------------------------------------------

@@ -34,6 +34,8 @@ cudaError_t launch_fwd_fp4(const FwdFp4Params& p, cudaStream_t st);
 cudaError_t launch_directp_codes(const float* s, long long n, float m, float c, const float* T,
                                  int native, uint8_t* codes, cudaStream_t st);
 
+cudaError_t launch_watchdog_selftest(unsigned* err, unsigned long long limit_ns, cudaStream_t st);
+
 // ---------------------------------------------------------------- BF16 fwd
 struct FwdBf16Params {
   CUtensorMap tm_q, tm_k, tm_v;     // bf16 Q, K, V

@@ -152,7 +152,26 @@ int grid_for(long long work, int per_cta) {
   return (int)(need < cap ? (need > 0 ? need : 1) : cap);
 }
 
+// One CTA waits, with a bounded wait, on an mbarrier that nothing arrives at:
+// the wait must expire, flag the device error word and return.
+__global__ void watchdog_selftest_kernel(unsigned* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  mbar_wait_ns(&bar, 0, &abort_flag, err, limit_ns);
+}
+
 }  // namespace
+
+cudaError_t launch_watchdog_selftest(unsigned* err, unsigned long long limit_ns, cudaStream_t st) {
+  watchdog_selftest_kernel<<<1, 32, 0, st>>>(err, limit_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quantize(const void* x, long long rows, int d, int N, long long BH, int fmt,
                             int axis, void* codes, void* scales, cudaStream_t st) {
