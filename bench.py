@@ -35,6 +35,9 @@ from precision_attention_fa4fp4_gb300.inputs import FWD_4K, SWEEP, TRAIN_8B, VID
 METRIC = "FP4 attention fwd TFLOP/s (noncausal, d=128) and speedup vs own BF16 kernel"
 FP4_OVER_BF16 = 13.5 / 2.25     # nominal dense FP4 : BF16 tensor rate on GB300
 FP8_OVER_BF16 = 4.5 / 2.25
+# DRAM read + write of one fwd_fp4_kernel<128> launch on this workload, from the
+# ncu capture summarised in profiles/fwd_fp4_kernel_noncausal_4k.md (same kernel).
+FWD_FP4_TRAFFIC_BYTES = 72.48e6
 
 
 def peaks():
@@ -275,7 +278,7 @@ def run_ours(args, rank, world, local):
         "quantize_ms": round(ms - fwd_mean, 4),
         "roofline": {"kernel": "fwd_fp4_kernel<128>", "bound": "tensor", "achieved": round(achieved, 1),
                      "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 4),
-                     "traffic": None,
+                     "traffic": FWD_FP4_TRAFFIC_BYTES,
                      "peak_source": f"{pk['source']} bf16 burst {pk['bf16']} TFLOP/s x nominal FP4/BF16 ratio 6"},
         "e2e": {"value": round(world * flops / (e2e_mean * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_mean, 4)},
