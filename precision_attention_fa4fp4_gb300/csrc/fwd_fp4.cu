@@ -8,22 +8,25 @@
 // product consumes (Consistent Normalization); MXFP4 for P and V (Format
 // Selection).  Q and K are MXFP4 as well.
 //
-// One CTA per (batch*head, 128-query tile), 18 warps:
-//   warp 0      producer: TMA loads of Q, K_j, V^T_j codes into swizzled shared
-//               memory; their E8M0 scales rearranged into the 32x16-byte chunks
-//               the scale-factor TMEM copy expects.
-//   warp 1      TMEM allocation; one lane issues tcgen05.cp (scale factors) and
-//               tcgen05.mma kind::mxf4 block_scale: S_j = Q K_j^T into a
-//               double-buffered S, O += P_j V_j, and l += P_j 1 (an N=16 MMA
-//               against an all-ones E2M1 tile, so the normalizer is summed by
-//               the tensor core from exactly the codes P V consumes).
-//   warps 2-17  softmax: 4 warps per TMEM lane quadrant; thread (row r, column
-//               group g) owns S[r][32g, 32g+32).  Row max exchanged through
-//               shared memory (one mbarrier per quadrant), Direct-P codes
-//               (native exponentials bracketed to the exact threshold map,
-//               threshold count where the bracket is ambiguous), eager O
-//               rescale of its 32 O columns, one 16-byte P chunk.
-// QK^T of tile j+1 runs on the tensor core while tile j's codes are built.
+// One CTA per (batch*head, pair of 128-query tiles A and B), 10 warps:
+//   warp 0      producer: TMA loads of Q_A, Q_B, K_j, V^T_j codes into swizzled
+//               shared memory; their E8M0 scales rearranged into the 32x16-byte
+//               chunks the scale-factor TMEM copy expects.  K_j and V_j are
+//               loaded once for both query tiles.
+//   warp 1      TMEM allocation; one elected lane issues tcgen05.cp (scale
+//               factors) and tcgen05.mma kind::mxf4 block_scale: S = Q_X K_j^T
+//               into one S buffer that the two query tiles take in turn,
+//               O_X += P_X V_j, and l_X += P_X 1 (an N=16 MMA against an
+//               all-ones E2M1 tile, so the normalizer is summed by the tensor
+//               core from exactly the codes P V consumes).
+//   warps 2-5   softmax of tile A, warps 6-9 softmax of tile B: one thread per
+//               query row (TMEM lane quadrant = warp mod 4), holding the row's
+//               128 scores of the key tile.  Row max, Direct-P codes (native
+//               exponentials bracketed to the exact threshold map, threshold
+//               count where the bracket is ambiguous), the row's 64-byte P
+//               chunk, eager rescale of the row of O_X and l_X.
+// While one tile's warps build codes, the other tile's S is computed and its
+// P V runs, so the latency of each hand-off hides behind the other tile's work.
 #include <cuda_bf16.h>
 #include "common.cuh"
 #include "internal.h"
@@ -31,14 +34,15 @@
 namespace fa4 {
 namespace {
 
-constexpr int BM = 128;         // queries per CTA
+constexpr int BM = 128;         // queries per tile; a CTA holds two tiles
 constexpr int BN = 128;         // keys per tile
 constexpr int STAGES = 6;       // K/V pipeline depth
-constexpr int NSOFT = 16;       // softmax warps
+constexpr int NSOFT = 8;        // softmax warps: 4 per query tile
 constexpr int NTHREADS = 32 * (2 + NSOFT);
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_L = 384, COL_SFQ = 400,
-                   COL_SFP = 404, COL_SFK = 408, COL_SFV = 408 + 4 * STAGES;
+// S at 0, O_X at 128 + 128X, l_X at 384 + 16X, scale factors from 416
+constexpr uint32_t COL_S = 0, COL_O0 = 128, COL_L0 = 384, COL_SFQ0 = 416, COL_SFP = 424,
+                   COL_SFK = 428, COL_SFV = 428 + 4 * STAGES;
 static_assert(COL_SFV + 4 * STAGES <= TMEM_COLS, "TMEM budget");
 
 template <int D>
@@ -48,17 +52,16 @@ struct Smem {
   static constexpr int VB = D * BN / 2;   // V^T: D rows of 128 keys
   static constexpr int PB = BM * BN / 2;
   static constexpr int ONESB = 16 * 64;   // 16 rows of 128 E2M1 ones
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + QB;
+  static constexpr int OFF_Q = 0;                          // Q_A, Q_B
+  static constexpr int OFF_K = OFF_Q + 2 * QB;
   static constexpr int OFF_V = OFF_K + STAGES * KB;
-  static constexpr int OFF_P = OFF_V + STAGES * VB;
-  static constexpr int OFF_ONES = OFF_P + 2 * PB;
+  static constexpr int OFF_P = OFF_V + STAGES * VB;        // [tile X][2 buffers]
+  static constexpr int OFF_ONES = OFF_P + 4 * PB;
   static constexpr int OFF_SF = OFF_ONES + ONESB;         // 512-byte scale chunks
-  static constexpr int SF_Q = OFF_SF, SF_P = SF_Q + 512, SF_K = SF_P + 512,
+  static constexpr int SF_Q = OFF_SF, SF_P = SF_Q + 1024, SF_K = SF_P + 512,
                        SF_V = SF_K + 512 * STAGES;
-  static constexpr int OFF_RED = SF_V + 512 * STAGES;     // float [2][4][128]
-  static constexpr int OFF_BAR = OFF_RED + 2 * 4 * 128 * 4;
-  static constexpr int NBAR = 1 + 4 * STAGES + 2 + 2 + 1 + 1 + 1 + 8;
+  static constexpr int OFF_BAR = SF_V + 512 * STAGES;
+  static constexpr int NBAR = 1 + 4 * STAGES + 2 + 2 + 2 + 2 + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int BYTES = OFF_MISC + 64 + 1024;    // + alignment slack
 };
@@ -143,25 +146,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
   uint64_t* k_empty = k_full + STAGES;
   uint64_t* v_full = k_empty + STAGES;
   uint64_t* v_empty = v_full + STAGES;
-  uint64_t* s_full = v_empty + STAGES;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* o_done = p_full + 1;
-  uint64_t* mma_done = o_done + 1;
-  uint64_t* red_bar = mma_done + 1;          // [2 parities][4 quadrants]
+  uint64_t* s_full = v_empty + STAGES;       // [X]: S holds Q_X K_j^T
+  uint64_t* s_free = s_full + 2;             // [X]: tile X's warps hold their S
+  uint64_t* p_full = s_free + 2;             // [X]: P_X written, O_X rescaled
+  uint64_t* o_done = p_full + 2;             // [X]: P_X V of the last tile done
+  uint64_t* mma_done = o_done + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
-  float* red = reinterpret_cast<float*>(smem + L::OFF_RED);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nq = (p.N + BM - 1) / BM;
-  const int qt = p.causal ? (nq - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+  const int npair = (nq + 1) / 2;
+  const int pair = p.causal ? (npair - 1 - (int)blockIdx.x) : (int)blockIdx.x;
   const int bh = blockIdx.y;
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int bkv = b * p.Hkv + h / (p.Hq / p.Hkv);
-  const int q0 = qt * BM;
+  const int q0 = pair * 2 * BM;              // first row of tile A; tile B follows
   const int nk_all = (p.N + BN - 1) / BN;
-  const int nt = p.causal ? min(nk_all, qt + 1) : nk_all;
+  // key tiles of the pair (tile A takes the last one fully masked when causal:
+  // its codes are all 0, so it adds exact zeros to O_A and l_A)
+  const int nt = p.causal ? min(nk_all, 2 * pair + 2) : nk_all;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -169,11 +173,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1);
       mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) { mbar_init(&s_full[s], 1); mbar_init(&s_free[s], NSOFT); }
-    mbar_init(p_full, NSOFT);
-    mbar_init(o_done, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&s_free[x], 4);
+      mbar_init(&p_full[x], 4);
+      mbar_init(&o_done[x], 1);
+    }
     mbar_init(mma_done, 1);
-    for (int i = 0; i < 8; ++i) mbar_init(&red_bar[i], 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -198,13 +204,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
     }
-    stage_sf_rows(smem + L::SF_Q, p.q_scales + (long long)bh * p.N * (D / 32), q0,
-                  min(BM, p.N - q0), D / 32, lane);
+    const uint8_t* qs = p.q_scales + (long long)bh * p.N * (D / 32);
+    stage_sf_rows(smem + L::SF_Q, qs, q0, min(BM, p.N - q0), D / 32, lane);
+    stage_sf_rows(smem + L::SF_Q + 512, qs, q0 + BM, min(BM, p.N - q0 - BM), D / 32, lane);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, L::QB);
+      mbar_arrive_expect_tx(q_full, 2 * L::QB);
       tma_load_3d(smem + L::OFF_Q, &p.tm_q, q_full, 0, q0, bh);
+      tma_load_3d(smem + L::OFF_Q + L::QB, &p.tm_q, q_full, 0, q0 + BM, bh);
     }
     const uint8_t* ks = p.k_scales + (long long)bkv * p.N * (D / 32);
     const uint8_t* vs = p.v_scales + (long long)bkv * D * (p.Np / 32);
@@ -259,189 +267,222 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr int KSTEPS = D / 64;   // K = 64 per mxf4 MMA
-      const uint32_t idesc_s = idesc_bs(BM, BN, 1, 1, false, false, 0, 0);
-      const uint32_t idesc_o = idesc_bs(BM, D, 1, 1, false, false, 0, 0);
-      const uint32_t idesc_l = idesc_bs(BM, 16, 1, 1, false, false, 0, 0);
-      constexpr Swizzle QSW = D == 128 ? SW_64B : SW_32B;
-      constexpr uint32_t QSBO = D == 128 ? 512 : 256;
-      const uint32_t sq = smem_u32(smem + L::OFF_Q);
-      const uint32_t sones = smem_u32(smem + L::OFF_ONES);
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
-      tc_fence_after();
-      if (ok) {
-        tmem_cp_sf(tbase + COL_SFQ, smem + L::SF_Q);
-        tmem_cp_sf(tbase + COL_SFP, smem + L::SF_P);
+    // The whole warp runs the schedule (waits, descriptor arithmetic) in
+    // uniform control flow; one elected lane issues each tcgen05 instruction.
+    const bool leader = elect_one();
+    constexpr int KSTEPS = D / 64;   // K = 64 per mxf4 MMA
+    const uint32_t idesc_s = idesc_bs(BM, BN, 1, 1, false, false, 0, 0);
+    const uint32_t idesc_o = idesc_bs(BM, D, 1, 1, false, false, 0, 0);
+    const uint32_t idesc_l = idesc_bs(BM, 16, 1, 1, false, false, 0, 0);
+    constexpr Swizzle QSW = D == 128 ? SW_64B : SW_32B;
+    constexpr uint32_t QSBO = D == 128 ? 512 : 256;
+    const uint32_t sq = smem_u32(smem + L::OFF_Q);
+    const uint32_t sones = smem_u32(smem + L::OFF_ONES);
+    bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
+    tc_fence_after();
+    if (ok && leader) {
+      tmem_cp_sf(tbase + COL_SFQ0, smem + L::SF_Q);
+      tmem_cp_sf(tbase + COL_SFQ0 + 4, smem + L::SF_Q + 512);
+      tmem_cp_sf(tbase + COL_SFP, smem + L::SF_P);
+    }
+    __syncwarp();
+    // S = Q_X K_t^T once the other tile's warps hold their S (first = no wait)
+    auto issue_qk = [&](int x, int t, bool first) -> bool {
+      const int st = t % STAGES;
+      if (x == 0) {
+        if (!mbar_wait(&k_full[st], (t / STAGES) & 1, abort_flag, p.err)) return false;
+        fence_proxy_async_smem();
+        tc_fence_after();
+        if (leader) tmem_cp_sf(tbase + COL_SFK + 4 * st, smem + L::SF_K + 512 * st);
+        __syncwarp();
       }
-      auto issue_pv = [&](int t) -> bool {
-        const int st = t % STAGES;
+      // the S buffer's last reader: tile B of t-1 (for A), tile A of t (for B)
+      if (!first && !mbar_wait(&s_free[x ^ 1], (x == 0 ? t - 1 : t) & 1, abort_flag, p.err)) return false;
+      tc_fence_after();
+      const uint32_t sqx = sq + x * L::QB;
+      const uint32_t sk = smem_u32(smem + L::OFF_K + st * L::KB);
+      if (leader) {
+#pragma unroll
+        for (int k = 0; k < KSTEPS; ++k) {
+          uint64_t ad = make_sdesc(sqx + 32 * k, 16, QSBO, QSW);
+          uint64_t bd = make_sdesc(sk + 32 * k, 16, QSBO, QSW);
+          uint32_t id = idesc_s | ((uint32_t)(2 * k) << 29) | ((uint32_t)(2 * k) << 4);
+          mma_mxf4(tbase + COL_S, ad, bd, id, tbase + COL_SFQ0 + 4 * x, tbase + COL_SFK + 4 * st, k > 0);
+        }
+        mma_commit(&s_full[x]);
+        if (x == 1) mma_commit(&k_empty[st]);
+      }
+      __syncwarp();
+      return true;
+    };
+    // O_X += P_X V_t, l_X += P_X 1
+    auto issue_pv = [&](int x, int t) -> bool {
+      const int st = t % STAGES;
+      if (x == 0) {
         if (!mbar_wait(&v_full[st], (t / STAGES) & 1, abort_flag, p.err)) return false;
         fence_proxy_async_smem();
-        tmem_cp_sf(tbase + COL_SFV + 4 * st, smem + L::SF_V + 512 * st);
-        if (!mbar_wait(p_full, t & 1, abort_flag, p.err)) return false;
-        tc_fence_after();
-        const uint32_t sp = smem_u32(smem + L::OFF_P + (t & 1) * L::PB);
-        const uint32_t sv = smem_u32(smem + L::OFF_V + st * L::VB);
+        if (leader) tmem_cp_sf(tbase + COL_SFV + 4 * st, smem + L::SF_V + 512 * st);
+        __syncwarp();
+      }
+      if (!mbar_wait(&p_full[x], t & 1, abort_flag, p.err)) return false;
+      tc_fence_after();
+      const uint32_t sp = smem_u32(smem + L::OFF_P + (2 * x + (t & 1)) * L::PB);
+      const uint32_t sv = smem_u32(smem + L::OFF_V + st * L::VB);
+      if (leader) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {     // 128 keys = 2 x K64
           const uint64_t ad = make_sdesc(sp + 32 * k, 16, 512, SW_64B);
           const uint32_t sf = ((uint32_t)(2 * k) << 29) | ((uint32_t)(2 * k) << 4);
-          mma_mxf4(tbase + COL_O, ad, make_sdesc(sv + 32 * k, 16, 512, SW_64B), idesc_o | sf,
+          mma_mxf4(tbase + COL_O0 + 128 * x, ad, make_sdesc(sv + 32 * k, 16, 512, SW_64B), idesc_o | sf,
                    tbase + COL_SFP, tbase + COL_SFV + 4 * st, t > 0 || k > 0);
-          mma_mxf4(tbase + COL_L, ad, make_sdesc(sones + 32 * k, 16, 512, SW_64B), idesc_l | sf,
+          mma_mxf4(tbase + COL_L0 + 16 * x, ad, make_sdesc(sones + 32 * k, 16, 512, SW_64B), idesc_l | sf,
                    tbase + COL_SFP, tbase + COL_SFP, t > 0 || k > 0);
         }
-        mma_commit(o_done);
-        mma_commit(&v_empty[st]);
-        return true;
-      };
-      for (int j = 0; ok && j < nt; ++j) {
-        const int st = j % STAGES;
-        if (!mbar_wait(&k_full[st], (j / STAGES) & 1, abort_flag, p.err)) { ok = false; break; }
-        fence_proxy_async_smem();
-        tc_fence_after();
-        tmem_cp_sf(tbase + COL_SFK + 4 * st, smem + L::SF_K + 512 * st);
-        const int sb = j & 1;
-        if (j >= 2 && !mbar_wait(&s_free[sb], ((j >> 1) - 1) & 1, abort_flag, p.err)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t sk = smem_u32(smem + L::OFF_K + st * L::KB);
-#pragma unroll
-        for (int k = 0; k < KSTEPS; ++k) {
-          uint64_t ad = make_sdesc(sq + 32 * k, 16, QSBO, QSW);
-          uint64_t bd = make_sdesc(sk + 32 * k, 16, QSBO, QSW);
-          uint32_t id = idesc_s | ((uint32_t)(2 * k) << 29) | ((uint32_t)(2 * k) << 4);
-          mma_mxf4(tbase + (sb ? COL_S1 : COL_S0), ad, bd, id, tbase + COL_SFQ, tbase + COL_SFK + 4 * st, k > 0);
-        }
-        mma_commit(&s_full[sb]);
-        mma_commit(&k_empty[st]);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        mma_commit(&o_done[x]);
+        if (x == 1) mma_commit(&v_empty[st]);
       }
-      if (ok && nt > 0) issue_pv(nt - 1);
-      mma_commit(mma_done);
-      volatile int no_abort = 0;
-      mbar_wait(mma_done, 0, &no_abort, p.err);
+      __syncwarp();
+      return true;
+    };
+    // Issue order follows the order the hand-offs arrive in: tile A loads S_j,
+    // so S_j of tile B is computed, then P_A V_{j-1}; tile B loads S_j, so
+    // S_{j+1} of tile A, then P_B V_{j-1}.  Each QK^T goes ahead of the P V
+    // that became ready just before it, since its tile waits for it first.
+    if (ok && nt > 0) ok = issue_qk(0, 0, true);
+    for (int j = 0; ok && j < nt; ++j) {
+      if (!issue_qk(1, j, false)) { ok = false; break; }
+      if (j > 0 && !issue_pv(0, j - 1)) { ok = false; break; }
+      if (j + 1 < nt && !issue_qk(0, j + 1, false)) { ok = false; break; }
+      if (j > 0 && !issue_pv(1, j - 1)) { ok = false; break; }
     }
+    if (ok && nt > 0) ok = issue_pv(0, nt - 1) && issue_pv(1, nt - 1);
+    if (leader) mma_commit(mma_done);
+    __syncwarp();
+    volatile int no_abort = 0;
+    mbar_wait(mma_done, 0, &no_abort, p.err);
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
+    const int x = (warp - 2) >> 2;            // query tile 0 (A) or 1 (B)
     const int quad = warp & 3;
-    const int g = (warp - 2) >> 2;            // column group 0..3
-    const int r = quad * 32 + lane;
-    const int qi = q0 + r;
+    const int r = quad * 32 + lane;           // row within the tile
+    const int qi = q0 + x * BM + r;
     const uint32_t lane_base = tbase + ((uint32_t)(quad * 32) << 16);
     const float c = p.c;
-    float T[7];
-#pragma unroll
-    for (int k = 0; k < 7; ++k) T[k] = p.T[k];
+    const float (&T)[7] = p.T;                // read from the parameter space
+    const int lim = p.causal ? min(p.N - 1, qi) : p.N - 1;   // last key of the row
+    const int sw = (r >> 1) & 3;              // 64-byte swizzle phase of row r
+    uint8_t* prow = smem + L::OFF_P + 2 * x * L::PB + r * 64;
     float m = -INFINITY;
     bool ok = true;
-    const int x = (r >> 1) & 3;               // 64-byte swizzle phase of row r
-    uint8_t* pchunk = smem + L::OFF_P + r * 64 + ((g ^ x) << 4);
     for (int j = 0; j < nt; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
+      if (!mbar_wait(&s_full[x], j & 1, abort_flag, p.err)) { ok = false; break; }
       tc_fence_after();
-      float s[32];
+      float s[4][32];
       {
-        uint32_t v[32];
-        tmem_ld32(lane_base + (sb ? COL_S1 : COL_S0) + 32 * g, v);
+        uint32_t v[4][32];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) tmem_ld32(lane_base + COL_S + 32 * g, v[g]);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(v[i]);
+        for (int g = 0; g < 4; ++g) {
+          reg_fence32(v[g]);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[g][i] = __uint_as_float(v[g][i]);
+        }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
-      const int kbase = j * BN + 32 * g;
-      if (j * BN + BN > p.N || (p.causal && j * BN + BN - 1 > q0)) {
-        const int lim = p.causal ? min(p.N - 1, qi) : p.N - 1;
+      if (lane == 0) mbar_arrive(&s_free[x]);
+      if (j * BN + BN - 1 > lim) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (kbase + i > lim) s[i] = -INFINITY;
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (j * BN + 32 * g + i > lim) s[g][i] = -INFINITY;
       }
-      float pm = fmax3(s[0], s[1], s[2]);
+      float mx = fmax3(s[0][0], s[0][1], s[0][2]);
 #pragma unroll
-      for (int i = 3; i + 1 < 32; i += 2) pm = fmax3(pm, s[i], s[i + 1]);
-      pm = fmaxf(pm, s[31]);
-      float* rslot = red + (sb * 4) * 128;
-      rslot[g * 128 + r] = pm;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&red_bar[sb * 4 + quad]);
-      if (!mbar_wait(&red_bar[sb * 4 + quad], (j >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
-      const float tmax = fmaxf(fmaxf(rslot[r], rslot[128 + r]), fmaxf(rslot[256 + r], rslot[384 + r]));
-      const float m_new = fmaxf(m, tmax);
+      for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int i = (g == 0 ? 3 : 0); i < 32; i += 2) mx = (i + 1 < 32) ? fmax3(mx, s[g][i], s[g][i + 1]) : fmaxf(mx, s[g][i]);
+      const float m_new = fmaxf(m, mx);
       const float mc = m_new * c;
-      uint32_t pw[4];
-      directp_codes32(s, c, mc, T, pw);
-      const float alpha = (m == -INFINITY) ? 1.f : ex2_approx(fmaf(m, c, -mc));
+      uint8_t* pb = prow + (j & 1) * L::PB;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint32_t pw[4];
+        directp_codes32(s[g], c, mc, T, pw);
+        *reinterpret_cast<uint4*>(pb + ((g ^ sw) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+      }
+      fence_proxy_async_smem();
       if (j > 0) {
-        if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+        // rescale O_X and l_X to the new max once P_X V of tile j-1 is in
+        if (!mbar_wait(&o_done[x], (j - 1) & 1, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
+        const float alpha = (m_new == m) ? 1.f : ex2_approx(fmaf(m, c, -mc));
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          if (32 * g < D) {
-            uint32_t v[32];
-            tmem_ld32(lane_base + COL_O + 32 * g, v);
+#pragma unroll
+          for (int g = 0; g < D / 32; ++g) {
+            uint32_t ov[32];
+            tmem_ld32(lane_base + COL_O0 + 128 * x + 32 * g, ov);
             tmem_ld_wait();
+            reg_fence32(ov);
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
-              float2 t = fmul2(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+              float2 t = fmul2(make_float2(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1])),
                                make_float2(alpha, alpha));
-              v[i] = __float_as_uint(t.x);
-              v[i + 1] = __float_as_uint(t.y);
+              ov[i] = __float_as_uint(t.x);
+              ov[i + 1] = __float_as_uint(t.y);
             }
-            tmem_st32(lane_base + COL_O + 32 * g, v);
+            tmem_st32(lane_base + COL_O0 + 128 * x + 32 * g, ov);
           }
-          if (g == 0) {
-            uint32_t lv = tmem_ld1(lane_base + COL_L);
-            tmem_ld_wait();
-            tmem_st1(lane_base + COL_L, __float_as_uint(__uint_as_float(lv) * alpha));
-          }
+          const uint32_t lv = tmem_ld1(lane_base + COL_L0 + 16 * x);
+          tmem_ld_wait();
+          tmem_st1(lane_base + COL_L0 + 16 * x, __float_as_uint(__uint_as_float(lv) * alpha));
           tmem_st_wait();
         }
       }
       m = m_new;
-      *reinterpret_cast<uint4*>(pchunk + sb * L::PB) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(&p_full[x]);
     }
-    if (ok && nt > 0 && mbar_wait(o_done, (nt - 1) & 1, abort_flag, p.err)) {
+    if (ok && nt > 0 && mbar_wait(&o_done[x], (nt - 1) & 1, abort_flag, p.err)) {
       tc_fence_after();
-      const float l = __uint_as_float(tmem_ld1(lane_base + COL_L));
+      const float l = __uint_as_float(tmem_ld1(lane_base + COL_L0 + 16 * x));
       tmem_ld_wait();
       const float inv_l = 1.f / l;
       const bool valid = qi < p.N;
-      const long long orow = ((long long)bh * p.N + qi) * D + 32 * g;
-      if (32 * g < D) {
+      const long long orow = ((long long)bh * p.N + qi) * D;
+#pragma unroll
+      for (int g = 0; g < D / 32; ++g) {
         uint32_t v[32];
-        tmem_ld32(lane_base + COL_O + 32 * g, v);
+        tmem_ld32(lane_base + COL_O0 + 128 * x + 32 * g, v);
         tmem_ld_wait();
-        if (valid) {
-          if (p.out_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow);
+        reg_fence32(v);
+        if (valid && p.out_bf16) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow + 32 * g);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t w[4];
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(v[q * 8 + 2 * e]) * inv_l,
-                                                         __uint_as_float(v[q * 8 + 2 * e + 1]) * inv_l);
-                w[e] = *reinterpret_cast<uint32_t*>(&t);
-              }
-              dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(v[q * 8 + 2 * e]) * inv_l,
+                                                       __uint_as_float(v[q * 8 + 2 * e + 1]) * inv_l);
+              w[e] = *reinterpret_cast<uint32_t*>(&t);
             }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + orow);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv_l, __uint_as_float(v[4 * q + 1]) * inv_l,
-                                   __uint_as_float(v[4 * q + 2]) * inv_l, __uint_as_float(v[4 * q + 3]) * inv_l);
+            dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
           }
+        } else if (valid) {
+          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + orow + 32 * g);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv_l, __uint_as_float(v[4 * q + 1]) * inv_l,
+                                 __uint_as_float(v[4 * q + 2]) * inv_l, __uint_as_float(v[4 * q + 3]) * inv_l);
         }
       }
-      if (g == 0 && valid && p.lse) p.lse[(long long)bh * p.N + qi] = p.scale * m + logf(l * (1.f / 6.f));
+      if (valid && p.lse) p.lse[(long long)bh * p.N + qi] = p.scale * m + logf(l * (1.f / 6.f));
     }
   }
   tc_fence_before();
@@ -496,7 +537,7 @@ __global__ void directp_codes_kernel(const float* __restrict__ s, long long n, f
 
 cudaError_t launch_fwd_fp4(const FwdFp4Params& p, cudaStream_t st) {
   const int nq = (p.N + BM - 1) / BM;
-  dim3 grid(nq, p.B * p.Hq);
+  dim3 grid((nq + 1) / 2, p.B * p.Hq);
   if (p.d == 128) {
     auto k = fwd_fp4_kernel<128>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<128>::BYTES);
