@@ -116,6 +116,18 @@ FA4_DEV void directp_codes32(const float (&s)[32], float c, float mc, const floa
   }
 }
 
+// Maximum of 128 values by a tree of fmax3 (short dependency chains).
+FA4_DEV float max128(const float (&s)[4][32]) {
+  float a[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) a[i] = fmax3(s[0][i], s[1][i], fmaxf(s[2][i], s[3][i]));
+#pragma unroll
+  for (int n = 32; n > 1; n /= 2)
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) a[i] = fmaxf(a[i], a[i + n / 2]);
+  return a[0];
+}
+
 // Rearrange 128 rows of per-row scale words into the scale-factor chunk:
 // chunk byte (r%32)*16 + (r/32)*4 + kblock.  Called by a full warp.
 FA4_DEV void stage_sf_rows(uint8_t* chunk, const uint8_t* src, int row0, int nrows_valid,
@@ -344,16 +356,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       __syncwarp();
       return true;
     };
-    // Issue order follows the order the hand-offs arrive in: tile A loads S_j,
-    // so S_j of tile B is computed, then P_A V_{j-1}; tile B loads S_j, so
-    // S_{j+1} of tile A, then P_B V_{j-1}.  Each QK^T goes ahead of the P V
-    // that became ready just before it, since its tile waits for it first.
+    // Issue order follows the order the hand-offs arrive in: tile A finishes
+    // tile j-1 (P_A V_{j-1}), then loads S_j (so S_j of tile B is computed);
+    // tile B finishes j-1 (P_B V_{j-1}), then loads S_j (S_{j+1} of tile A).
+    // P V goes first so the rescale in the tile's next step finds it done; the
+    // other tile needs its S only half a step later.
     if (ok && nt > 0) ok = issue_qk(0, 0, true);
     for (int j = 0; ok && j < nt; ++j) {
-      if (!issue_qk(1, j, false)) { ok = false; break; }
       if (j > 0 && !issue_pv(0, j - 1)) { ok = false; break; }
-      if (j + 1 < nt && !issue_qk(0, j + 1, false)) { ok = false; break; }
+      if (!issue_qk(1, j, false)) { ok = false; break; }
       if (j > 0 && !issue_pv(1, j - 1)) { ok = false; break; }
+      if (j + 1 < nt && !issue_qk(0, j + 1, false)) { ok = false; break; }
     }
     if (ok && nt > 0) ok = issue_pv(0, nt - 1) && issue_pv(1, nt - 1);
     if (leader) mma_commit(mma_done);
@@ -401,12 +414,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
           for (int i = 0; i < 32; ++i)
             if (j * BN + 32 * g + i > lim) s[g][i] = -INFINITY;
       }
-      float mx = fmax3(s[0][0], s[0][1], s[0][2]);
-#pragma unroll
-      for (int g = 0; g < 4; ++g)
-#pragma unroll
-        for (int i = (g == 0 ? 3 : 0); i < 32; i += 2) mx = (i + 1 < 32) ? fmax3(mx, s[g][i], s[g][i + 1]) : fmaxf(mx, s[g][i]);
-      const float m_new = fmaxf(m, mx);
+      const float m_new = fmaxf(m, max128(s));
       const float mc = m_new * c;
       uint8_t* pb = prow + (j & 1) * L::PB;
 #pragma unroll
