@@ -26,6 +26,9 @@
 //                blocks of 32 keys (warp-wide max with redux.sync).
 //   warps 10-13  dQ^T from TMEM, times softmax_scale, added into dq.
 //   After the loop: dV and dK * softmax_scale written by warps 2-9.
+// The P/dS warps release S^T and dP^T as soon as they hold them in registers,
+// so S^T and dP^T of step t+1 run on the tensor core while step t's P and dS
+// are built; P, dS and their scale chunks are double-buffered by step parity.
 #include <cuda_bf16.h>
 #include "common.cuh"
 #include "internal.h"
@@ -35,6 +38,7 @@ namespace {
 
 constexpr int BK = 128;          // keys per CTA
 constexpr int BQ = 64;           // queries per step
+constexpr int NST = 4;           // input stages (Q4, dOr, Q8, dOc of a step)
 constexpr int D = 128;
 constexpr int NTHREADS = 14 * 32;
 constexpr uint32_t TMEM_COLS = 512;
@@ -50,14 +54,15 @@ struct BL {   // shared-memory layout (bytes)
   static constexpr int STG = K8 + D * BK;            // stages
   static constexpr int Q4 = 0, DOR = Q4 + BQ * D / 2, Q8 = DOR + BQ * D, DOC = Q8 + D * BQ;
   static constexpr int STAGE_BYTES = DOC + D * BQ;   // 28 KB
-  static constexpr int PQ = STG + 2 * STAGE_BYTES;   // 128 keys x 64 B
-  static constexpr int DSC = PQ + BK * BQ;
-  static constexpr int DSR = DSC + BK * BQ;
-  static constexpr int SFC = DSR + BK * BQ;          // scale chunks, 512 B each
-  // chunk ids: 0 K4, 1 V8, 2 K8, 3 P, 4 dSc, 5 dSr, 6-7 Q4, 8-9 dOr, 10-11 Q8, 12-13 dOc
-  static constexpr int VEC = SFC + 14 * 512;         // float lse2[2][64], dvec[2][64]
-  static constexpr int BAR = VEC + 4 * BQ * 4;
-  static constexpr int NBAR = 1 + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 1;
+  static constexpr int PQ = STG + NST * STAGE_BYTES; // [2] x 128 keys x 64 B
+  static constexpr int DSC = PQ + 2 * BK * BQ;       // [2]
+  static constexpr int DSR = DSC + 2 * BK * BQ;      // [2]
+  static constexpr int SFC = DSR + 2 * BK * BQ;      // scale chunks, 512 B each
+  // chunk ids: 0 K4, 1 V8, 2 K8, 3-4 P, 5-6 dSc, 7-8 dSr (by step parity),
+  // 9 + 4 * stage + {0 Q4, 1 dOr, 2 Q8, 3 dOc}
+  static constexpr int VEC = SFC + (9 + 4 * NST) * 512;   // float lse2[NST][64], dvec[NST][64]
+  static constexpr int BAR = VEC + 2 * NST * BQ * 4;
+  static constexpr int NBAR = 1 + NST + NST + 1 + 1 + 2 + 1 + 1 + 1 + 1;
   static constexpr int MISC = BAR + 8 * NBAR;
   static constexpr int BYTES = MISC + 64 + 1024;
 };
@@ -110,19 +115,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BL::BAR);
   uint64_t* fix_full = bars;
-  uint64_t* in_full = bars + 1;
-  uint64_t* in_empty = bars + 3;
-  uint64_t* s_full = bars + 5;
-  uint64_t* p_full = bars + 6;
-  uint64_t* dq_full = bars + 7;
-  uint64_t* dq_free = bars + 8;
-  uint64_t* acc_done = bars + 9;
-  uint64_t* mma_done = bars + 10;
+  uint64_t* in_full = bars + 1;               // [NST]
+  uint64_t* in_empty = in_full + NST;         // [NST]
+  uint64_t* s_full = in_empty + NST;
+  uint64_t* st_free = s_full + 1;             // the P/dS warps hold S^T, dP^T
+  uint64_t* p_full = st_free + 1;             // [2]: P, dS of a step written
+  uint64_t* dq_full = p_full + 2;
+  uint64_t* dq_free = dq_full + 1;
+  uint64_t* acc_done = dq_free + 1;
+  uint64_t* mma_done = acc_done + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + BL::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + BL::MISC + 4);
   uint8_t* sfc = smem + BL::SFC;
   float* lse2 = reinterpret_cast<float*>(smem + BL::VEC);     // [2][64]
-  float* dvec = lse2 + 2 * BQ;                                 // [2][64]
+  float* dvec = lse2 + NST * BQ;                               // [NST][64]
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int kt = blockIdx.x;
@@ -137,9 +143,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
 
   if (threadIdx.x == 0) {
     mbar_init(fix_full, 1);
-    for (int s = 0; s < 2; ++s) { mbar_init(&in_full[s], 1); mbar_init(&in_empty[s], 1); }
+    for (int s = 0; s < NST; ++s) { mbar_init(&in_full[s], 1); mbar_init(&in_empty[s], 1); }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 8);
+    mbar_init(st_free, 8);
+    mbar_init(&p_full[0], 8);
+    mbar_init(&p_full[1], 8);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 4);
     mbar_init(acc_done, 1);
@@ -169,16 +177,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
     }
     int issued = 0;
     for (int t = 0; t < nsteps; ++t) {
-      const int st = t & 1;
+      const int st = t % NST;
       const int h = hk * group + t / per_head;
       const int q0 = (i0 + t % per_head) * BQ;
       const int bh = b * p.Hq + h;
-      if (t >= 2 && !mbar_wait(&in_empty[st], ((t >> 1) - 1) & 1, abort_flag, p.err)) break;
+      if (t >= NST && !mbar_wait(&in_empty[st], ((t / NST) - 1) & 1, abort_flag, p.err)) break;
       const int nq_valid = min(BQ, p.N - q0);
-      stage_chunk(sfc + (6 + st) * 512, p.q4_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, 4, lane);
-      stage_chunk(sfc + (8 + st) * 512, p.do_r_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, 4, lane);
-      stage_chunk(sfc + (10 + st) * 512, p.q8c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
-      stage_chunk(sfc + (12 + st) * 512, p.do_c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
+      uint8_t* sc = sfc + (9 + 4 * st) * 512;
+      stage_chunk(sc, p.q4_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, 4, lane);
+      stage_chunk(sc + 512, p.do_r_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, 4, lane);
+      stage_chunk(sc + 1024, p.q8c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
+      stage_chunk(sc + 1536, p.do_c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int qq = lane + 32 * u;
@@ -206,85 +215,105 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
     if (*abort_flag && lane == 0) {
       volatile int no_abort = 0;
       mbar_wait(fix_full, 0, &no_abort, p.err);
-      for (int t = max(0, issued - 2); t < issued; ++t) mbar_wait(&in_full[t & 1], (t >> 1) & 1, &no_abort, p.err);
+      for (int t = max(0, issued - NST); t < issued; ++t) mbar_wait(&in_full[t % NST], (t / NST) & 1, &no_abort, p.err);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t id_st = idesc_bs(128, BQ, 1, 1, false, false, 0, 0);      // mxf4
-      const uint32_t id_dp = idesc_bs(128, BQ, 0, 0, false, false, 0, 0);      // mxf8 e4m3
-      const uint32_t id_acc = idesc_bs(128, D, 0, 0, false, false, 0, 0);
-      const uint32_t id_dq = idesc_bs(128, BQ, 0, 0, false, true, 0, 0);
-      const uint32_t s_k4 = smem_u32(smem + BL::K4), s_v8 = smem_u32(smem + BL::V8),
-                     s_k8 = smem_u32(smem + BL::K8), s_pq = smem_u32(smem + BL::PQ),
-                     s_dsc = smem_u32(smem + BL::DSC), s_dsr = smem_u32(smem + BL::DSR);
-      bool ok = mbar_wait(fix_full, 0, abort_flag, p.err);
+    // The whole warp runs the schedule in uniform control flow; one elected
+    // lane issues each tcgen05 instruction.
+    const bool leader = elect_one();
+    const uint32_t id_st = idesc_bs(128, BQ, 1, 1, false, false, 0, 0);      // mxf4
+    const uint32_t id_dp = idesc_bs(128, BQ, 0, 0, false, false, 0, 0);      // mxf8 e4m3
+    const uint32_t id_acc = idesc_bs(128, D, 0, 0, false, false, 0, 0);
+    const uint32_t id_dq = idesc_bs(128, BQ, 0, 0, false, true, 0, 0);
+    const uint32_t s_k4 = smem_u32(smem + BL::K4), s_v8 = smem_u32(smem + BL::V8),
+                   s_k8 = smem_u32(smem + BL::K8), s_pq = smem_u32(smem + BL::PQ),
+                   s_dsc = smem_u32(smem + BL::DSC), s_dsr = smem_u32(smem + BL::DSR);
+    bool ok = mbar_wait(fix_full, 0, abort_flag, p.err);
+    tc_fence_after();
+    if (ok && leader) {
+      tmem_cp_sf(tbase + SF_K4, sfc + 0 * 512);
+      tmem_cp_sf(tbase + SF_V8, sfc + 1 * 512);
+      tmem_cp_sf(tbase + SF_K8, sfc + 2 * 512);
+    }
+    __syncwarp();
+    // S^T(t) = K4 Q4^T and dP^T(t) = V8r dOr^T, into TMEM the P/dS warps have
+    // released (first = nothing to wait for)
+    auto issue_sdp = [&](int t, bool first) -> bool {
+      const int st = t % NST, sp = t & 1;     // input stage; TMEM scale slot
+      if (!mbar_wait(&in_full[st], (t / NST) & 1, abort_flag, p.err)) return false;
+      if (!first && !mbar_wait(st_free, (t - 1) & 1, abort_flag, p.err)) return false;
       tc_fence_after();
-      if (ok) {
-        tmem_cp_sf(tbase + SF_K4, sfc + 0 * 512);
-        tmem_cp_sf(tbase + SF_V8, sfc + 1 * 512);
-        tmem_cp_sf(tbase + SF_K8, sfc + 2 * 512);
-      }
-      for (int t = 0; ok && t < nsteps; ++t) {
-        const int st = t & 1;
-        if (!mbar_wait(&in_full[st], (t >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t sb = smem_u32(smem + BL::STG + st * BL::STAGE_BYTES);
-        tmem_cp_sf(tbase + SF_Q4 + 4 * st, sfc + (6 + st) * 512);
-        tmem_cp_sf(tbase + SF_DOR + 4 * st, sfc + (8 + st) * 512);
-        tmem_cp_sf(tbase + SF_Q8 + 4 * st, sfc + (10 + st) * 512);
-        tmem_cp_sf(tbase + SF_DOC + 4 * st, sfc + (12 + st) * 512);
-        // S^T = K4 Q4^T (K = d = 128: 2 x K64)
+      const uint32_t sb = smem_u32(smem + BL::STG + st * BL::STAGE_BYTES);
+      if (leader) {
+        const uint8_t* sc = sfc + (9 + 4 * st) * 512;
+        tmem_cp_sf(tbase + SF_Q4 + 4 * sp, sc);
+        tmem_cp_sf(tbase + SF_DOR + 4 * sp, sc + 512);
+        tmem_cp_sf(tbase + SF_Q8 + 4 * sp, sc + 1024);
+        tmem_cp_sf(tbase + SF_DOC + 4 * sp, sc + 1536);
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < 2; ++k) {     // K = d = 128: 2 x K64
           const uint32_t sf = ((uint32_t)(2 * k) << 29) | ((uint32_t)(2 * k) << 4);
           mma_mxf4(tbase + COL_ST, make_sdesc(s_k4 + 32 * k, 16, 512, SW_64B),
                    make_sdesc(sb + BL::Q4 + 32 * k, 16, 512, SW_64B), id_st | sf, tbase + SF_K4,
-                   tbase + SF_Q4 + 4 * st, k > 0);
+                   tbase + SF_Q4 + 4 * sp, k > 0);
         }
-        // dP^T = V8r dOr^T (K = d: 4 x K32)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 4; ++k) {     // K = d: 4 x K32
           const uint32_t sf = ((uint32_t)k << 29) | ((uint32_t)k << 4);
           mma_mxf8(tbase + COL_DPT, make_sdesc(s_v8 + 32 * k, 16, 1024, SW_128B),
                    make_sdesc(sb + BL::DOR + 32 * k, 16, 1024, SW_128B), id_dp | sf, tbase + SF_V8,
-                   tbase + SF_DOR + 4 * st, k > 0);
+                   tbase + SF_DOR + 4 * sp, k > 0);
         }
         mma_commit(s_full);
-        if (!mbar_wait(p_full, t & 1, abort_flag, p.err)) { ok = false; break; }
-        tc_fence_after();
-        tmem_cp_sf(tbase + SF_P, sfc + 3 * 512);
-        tmem_cp_sf(tbase + SF_DSC, sfc + 4 * 512);
-        tmem_cp_sf(tbase + SF_DSR, sfc + 5 * 512);
+      }
+      __syncwarp();
+      return true;
+    };
+    if (ok && nsteps > 0) ok = issue_sdp(0, true);
+    for (int t = 0; ok && t < nsteps; ++t) {
+      const int st = t % NST, sp = t & 1;
+      if (t + 1 < nsteps && !issue_sdp(t + 1, false)) { ok = false; break; }
+      if (!mbar_wait(&p_full[sp], (t >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
+      tc_fence_after();
+      if (t >= 1 && !mbar_wait(dq_free, (t - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sb = smem_u32(smem + BL::STG + st * BL::STAGE_BYTES);
+      if (leader) {
+        tmem_cp_sf(tbase + SF_P, sfc + (3 + sp) * 512);
+        tmem_cp_sf(tbase + SF_DSC, sfc + (5 + sp) * 512);
+        tmem_cp_sf(tbase + SF_DSR, sfc + (7 + sp) * 512);
         // dV += Pq^T dOc, dK += dSc^T Q8c (K = 64 queries: 2 x K32)
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           const uint32_t sf = ((uint32_t)k << 29) | ((uint32_t)k << 4);
-          mma_mxf8(tbase + COL_DV, make_sdesc(s_pq + 32 * k, 16, 512, SW_64B),
+          mma_mxf8(tbase + COL_DV, make_sdesc(s_pq + sp * BK * BQ + 32 * k, 16, 512, SW_64B),
                    make_sdesc(sb + BL::DOC + 32 * k, 16, 512, SW_64B), id_acc | sf, tbase + SF_P,
-                   tbase + SF_DOC + 4 * st, t > 0 || k > 0);
-          mma_mxf8(tbase + COL_DK, make_sdesc(s_dsc + 32 * k, 16, 512, SW_64B),
+                   tbase + SF_DOC + 4 * sp, t > 0 || k > 0);
+          mma_mxf8(tbase + COL_DK, make_sdesc(s_dsc + sp * BK * BQ + 32 * k, 16, 512, SW_64B),
                    make_sdesc(sb + BL::Q8 + 32 * k, 16, 512, SW_64B), id_acc | sf, tbase + SF_DSC,
-                   tbase + SF_Q8 + 4 * st, t > 0 || k > 0);
+                   tbase + SF_Q8 + 4 * sp, t > 0 || k > 0);
         }
         // dQ^T = K8c^T dSr (K = 128 keys: 4 x K32; dSr stored [keys][64 q], MN-major)
-        if (t >= 1 && !mbar_wait(dq_free, (t - 1) & 1, abort_flag, p.err)) { ok = false; break; }
-        tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint32_t sf = ((uint32_t)k << 29) | ((uint32_t)k << 4);
           mma_mxf8(tbase + COL_DQT, make_sdesc(s_k8 + 32 * k, 16, 1024, SW_128B),
-                   make_sdesc(s_dsr + 2048 * k, 8192, 512, SW_64B), id_dq | sf, tbase + SF_K8,
-                   tbase + SF_DSR, k > 0);
+                   make_sdesc(s_dsr + sp * BK * BQ + 2048 * k, 8192, 512, SW_64B), id_dq | sf,
+                   tbase + SF_K8, tbase + SF_DSR, k > 0);
         }
         mma_commit(dq_full);
         mma_commit(&in_empty[st]);
       }
+      __syncwarp();
+    }
+    if (leader) {
       mma_commit(acc_done);
       mma_commit(mma_done);
-      volatile int no_abort = 0;
-      mbar_wait(mma_done, 0, &no_abort, p.err);
     }
+    __syncwarp();
+    volatile int no_abort = 0;
+    mbar_wait(mma_done, 0, &no_abort, p.err);
     __syncwarp();
   } else if (warp < 10) {
     // ------------------------------------------------------------ P / dS
@@ -295,28 +324,34 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
     const uint32_t lane_base = tbase + ((uint32_t)(quad * 32) << 16);
     const float c = p.c;
     bool ok = true;
-    uint8_t* pq = smem + BL::PQ;
-    uint8_t* dsc = smem + BL::DSC;
-    uint8_t* dsr = smem + BL::DSR;
+    uint8_t* const pq0 = smem + BL::PQ;
+    uint8_t* const dsc0 = smem + BL::DSC;
+    uint8_t* const dsr0 = smem + BL::DSR;
     for (int t = 0; t < nsteps; ++t) {
-      const int st = t & 1;
+      const int st = t % NST, sp = t & 1;     // input stage; P/dS buffer
       const int q0 = (i0 + t % per_head) * BQ;
+      uint8_t* pq = pq0 + sp * BK * BQ;
+      uint8_t* dsc = dsc0 + sp * BK * BQ;
+      uint8_t* dsr = dsr0 + sp * BK * BQ;
       if (!mbar_wait(s_full, t & 1, abort_flag, p.err)) { ok = false; break; }
       // LSE / D of this stage were written by the producer's threads
-      if (!mbar_wait(&in_full[st], (t >> 1) & 1, abort_flag, p.err)) { ok = false; break; }
+      if (!mbar_wait(&in_full[st], (t / NST) & 1, abort_flag, p.err)) { ok = false; break; }
       tc_fence_after();
       float s[32], dp[32];
       {
-        uint32_t v[32];
+        uint32_t v[32], w[32];
         tmem_ld32(lane_base + COL_ST + 32 * g, v);
+        tmem_ld32(lane_base + COL_DPT + 32 * g, w);
         tmem_ld_wait();
+        reg_fence32(v);
+        reg_fence32(w);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(v[i]);
-        tmem_ld32(lane_base + COL_DPT + 32 * g, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) dp[i] = __uint_as_float(v[i]);
+        for (int i = 0; i < 32; ++i) { s[i] = __uint_as_float(v[i]); dp[i] = __uint_as_float(w[i]); }
       }
+      // S^T and dP^T are in registers: the tensor core may overwrite them
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(st_free);
       const float* l2v = lse2 + st * BQ + 32 * g;
       const float* dv = dvec + st * BQ + 32 * g;
       const int qbase = q0 + 32 * g;
@@ -341,8 +376,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
       const int xc = e4m3_block_exp(dsmax, &inv);
       e4m3x32(dp, inv, lo, hi);
       st_row_sw64(dsc, r, g, lo, hi);
-      sfc[3 * 512 + lane * 16 + quad * 4 + g] = (uint8_t)(xp + 127);
-      sfc[4 * 512 + lane * 16 + quad * 4 + g] = (uint8_t)(xc + 127);
+      sfc[(3 + sp) * 512 + lane * 16 + quad * 4 + g] = (uint8_t)(xp + 127);
+      sfc[(5 + sp) * 512 + lane * 16 + quad * 4 + g] = (uint8_t)(xc + 127);
       // dS in blocks of 32 keys (the 32 lanes of this warp) per query column
       float q8[32];
       uint32_t my_scale = 0;
@@ -356,11 +391,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
       }
       e4m3x32(q8, 1.f, lo, hi);
       st_row_sw64(dsr, r, g, lo, hi);
-      sfc[5 * 512 + lane * 16 + g * 4 + quad] = (uint8_t)my_scale;
+      sfc[(7 + sp) * 512 + lane * 16 + g * 4 + quad] = (uint8_t)my_scale;
       fence_proxy_async_smem();
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(&p_full[sp]);
     }
     // dV, dK out
     if (ok && mbar_wait(acc_done, 0, abort_flag, p.err)) {
@@ -393,7 +427,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
   } else {
     // ------------------------------------------------------------ dQ writer
     const int quad = warp & 3;
-    const int drow = quad * 32 + lane;
     const uint32_t lane_base = tbase + ((uint32_t)(quad * 32) << 16);
     for (int t = 0; t < nsteps; ++t) {
       const int h = hk * group + t / per_head;
@@ -404,17 +437,41 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
       tmem_ld32(lane_base + COL_DQT, v0);
       tmem_ld32(lane_base + COL_DQT + 32, v1);
       tmem_ld_wait();
+      reg_fence32(v0);
+      reg_fence32(v1);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_free);
-      float* dst = p.dq + ((long long)(b * p.Hq + h) * p.N + q0) * D + drow;
+      // Thread (d row 32*quad + lane) holds dQ[q0 + i][d] for 64 queries i.
+      // 4x4 transposes among the lanes 4a..4a+3 (two butterfly exchanges)
+      // give lane 4a+b the values d = 32*quad + 4a .. +3 of query 4*blk + b,
+      // added into dq with one 16-byte atomic.
+      const int bq = lane & 3, a4 = lane & ~3;
+      float* dst = p.dq + ((long long)(b * p.Hq + h) * p.N + q0) * D + quad * 32 + a4;
       const int nq = min(BQ, p.N - q0);
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < nq) atomicAdd(dst + (long long)i * D, __uint_as_float(v0[i]) * p.scale);
+      for (int blk = 0; blk < 16; ++blk) {
+        float e[4];
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (32 + i < nq) atomicAdd(dst + (long long)(32 + i) * D, __uint_as_float(v1[i]) * p.scale);
+        for (int c = 0; c < 4; ++c) {
+          const int i = 4 * blk + c;
+          e[c] = __uint_as_float(i < 32 ? v0[i] : v1[i - 32]) * p.scale;
+        }
+#pragma unroll
+        for (int k = 1; k <= 2; k <<= 1) {
+          const bool hi = (lane & k) != 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (i & k) continue;
+            const int j = i | k;
+            const float send = hi ? e[i] : e[j];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, k);
+            if (hi) e[i] = recv; else e[j] = recv;
+          }
+        }
+        const int qi = 4 * blk + bq;
+        if (qi < nq) atomicAdd(reinterpret_cast<float4*>(dst + (long long)qi * D), make_float4(e[0], e[1], e[2], e[3]));
+      }
     }
   }
   tc_fence_before();
