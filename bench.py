@@ -36,9 +36,9 @@ METRIC = "FP4 attention fwd TFLOP/s (noncausal, d=128) and speedup vs own BF16 k
 FP4_OVER_BF16 = 13.5 / 2.25     # nominal dense FP4 : BF16 tensor rate on GB300
 FP8_OVER_BF16 = 4.5 / 2.25
 # DRAM read + write of one fwd_fp4_kernel<128> launch on this workload, from the
-# ncu capture summarised in profiles/fwd_fp4_kernel_noncausal_4k.md; None while
-# that capture predates the kernel as built.
-FWD_FP4_TRAFFIC_BYTES = None
+# ncu capture summarised in profiles/fwd_fp4_kernel_noncausal_4k.md (same kernel;
+# set to None whenever the kernel changes after the capture).
+FWD_FP4_TRAFFIC_BYTES = 71.82e6
 
 
 def peaks():
