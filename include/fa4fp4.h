@@ -80,6 +80,19 @@ FA4FP4_API size_t fa4fp4_qtensor_bytes(int B, int H, int N, int d, int fmt, int 
 FA4FP4_API fa4fp4_status fa4fp4_quantize(const void* x_bf16, int B, int H, int N, int d, int fmt, int axis,
                               void* codes, void* scales, void* stream);
 
+/* The three forward inputs in one launch: q [B][Hq][N][d] and k [B][Hkv][N][d]
+ * to MXFP4 with blocks along d, v [B][Hkv][N][d] to MXFP4 with blocks along N
+ * (the transposed V^T layout), byte for byte what fa4fp4_quantize writes for
+ * each of them (same rule, layouts and sizes: fa4fp4_qtensor_bytes);
+ * technical summary, Methodology 1 ("Format Selection": MXFP4 Q, K and V).
+ * The transposes of V share the grid with the row blocks of Q and K.  All
+ * buffers are device memory owned by the caller, 16-byte aligned; errors as
+ * fa4fp4_fwd's dimension checks (d in {64,128}, Hq a multiple of Hkv). */
+FA4FP4_API fa4fp4_status fa4fp4_quantize_qkv(const void* q_bf16, const void* k_bf16, const void* v_bf16,
+                                             int B, int Hq, int Hkv, int N, int d, void* q_codes,
+                                             void* q_scales, void* k_codes, void* k_scales,
+                                             void* vt_codes, void* vt_scales, void* stream);
+
 /* Direct-P forward (technical summary, Methodology 1 "Direct Mapping" and
  * "Consistent Normalization"; abstract).
  *   q: MXFP4 along d, [B][Hq][N][d];  k: MXFP4 along d, [B][Hkv][N][d];

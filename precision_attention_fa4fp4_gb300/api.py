@@ -50,6 +50,8 @@ def load_library():
         lib.fa4fp4_qtensor_bytes.argtypes = [i, i, i, i, i, i, ctypes.POINTER(sz)]
         lib.fa4fp4_quantize.restype = i
         lib.fa4fp4_quantize.argtypes = [vp, i, i, i, i, i, i, vp, vp, vp]
+        lib.fa4fp4_quantize_qkv.restype = i
+        lib.fa4fp4_quantize_qkv.argtypes = [vp, vp, vp, i, i, i, i, i] + [vp] * 7
         lib.fa4fp4_fwd.restype = i
         lib.fa4fp4_fwd.argtypes = [vp] * 6 + [i, i, i, i, i, f, i, vp, i, vp, vp]
         lib.fa4fp4_bwd_workspace_bytes.restype = sz
@@ -126,6 +128,28 @@ def quantize(x: torch.Tensor, fmt: int = FMT_MXFP4, axis: int = ALONG_D, out: QT
     _check("fa4fp4_quantize", load_library().fa4fp4_quantize(
         _ptr(x), B, H, N, d, fmt, axis, _ptr(q.codes), _ptr(q.scales), _stream(x.device)))
     return q
+
+
+def quantize_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out=None):
+    """Q, K (MXFP4 along d) and V (MXFP4 along N) in one launch
+    (fa4fp4_quantize_qkv).  Returns (q4, k4, vt) as quantize would."""
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or t.dim() != 4:
+            raise ValueError("quantize_qkv expects bf16 [B,H,N,d] tensors")
+        _cuda(t)
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, N, d) or v.shape != k.shape:
+        raise ValueError("quantize_qkv: k and v must be [B,Hkv,N,d] with q's B, N, d")
+    if out is None:
+        out = (qtensor_alloc(B, Hq, N, d, FMT_MXFP4, ALONG_D, q.device),
+               qtensor_alloc(B, Hkv, N, d, FMT_MXFP4, ALONG_D, q.device),
+               qtensor_alloc(B, Hkv, N, d, FMT_MXFP4, ALONG_N, q.device))
+    q4, k4, vt = out
+    _check("fa4fp4_quantize_qkv", load_library().fa4fp4_quantize_qkv(
+        _ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, N, d, _ptr(q4.codes), _ptr(q4.scales), _ptr(k4.codes),
+        _ptr(k4.scales), _ptr(vt.codes), _ptr(vt.scales), _stream(q.device)))
+    return q4, k4, vt
 
 
 def fwd(q: QTensor, k: QTensor, vt: QTensor, causal: bool = False, softmax_scale: float = 0.0,

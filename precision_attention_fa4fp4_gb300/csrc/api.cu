@@ -142,6 +142,22 @@ fa4fp4_status fa4fp4_quantize(const void* x, int B, int H, int N, int d, int fmt
                                        static_cast<cudaStream_t>(stream)));
 }
 
+fa4fp4_status fa4fp4_quantize_qkv(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,
+                                  int N, int d, void* q_codes, void* q_scales, void* k_codes, void* k_scales,
+                                  void* vt_codes, void* vt_scales, void* stream) {
+  if (!q || !k || !v || !q_codes || !q_scales || !k_codes || !k_scales || !vt_codes || !vt_scales)
+    return FA4FP4_ERR_INVALID_ARG;
+  fa4fp4_status s = check_dims(B, Hq, Hkv, N, d);
+  if (s != FA4FP4_OK) return s;
+  const void* ptrs[] = {q, k, v, q_codes, q_scales, k_codes, k_scales, vt_codes, vt_scales};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return FA4FP4_ERR_ALIGNMENT;
+  if (B == 0 || Hq == 0) return FA4FP4_OK;
+  return launch_status(launch_quantize_qkv(q, k, v, (long long)B * Hq, (long long)B * Hkv, N, d, q_codes,
+                                           q_scales, k_codes, k_scales, vt_codes, vt_scales,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 fa4fp4_status fa4fp4_fwd(const void* qc, const void* qs, const void* kc, const void* ks,
                          const void* vc, const void* vs, int B, int Hq, int Hkv, int N, int d,
                          float softmax_scale, int causal, void* o, int out_dtype, float* lse,

@@ -14,6 +14,21 @@ struct Thresh { float v[7]; };
 inline int padded_n(int N) { return (N + 127) / 128 * 128; }
 
 // ---------------------------------------------------------------- quantize
+// Q, K (MXFP4 along d) and V (MXFP4 along N) in one launch.
+struct QkvParams {
+  const uint4* q;
+  const uint4* k;
+  const void* v;               // bf16
+  uint8_t *qc, *qs, *kc, *ks, *vc, *vs;
+  int N, Np;
+  long long nbq, nbk;          // 32-element blocks of Q and K
+  long long nq_cta, nk_cta;    // CTAs of 256 row blocks
+  long long nv;                // 128-token V tiles
+  long long period;            // every period-th CTA (of the first nv) is a V tile
+};
+cudaError_t launch_quantize_qkv(const void* q, const void* k, const void* v, long long BHq, long long BHkv,
+                                int N, int d, void* qc, void* qs, void* kc, void* ks, void* vc, void* vs,
+                                cudaStream_t st);
 cudaError_t launch_quantize(const void* x, long long rows, int d, int N, long long BH, int fmt,
                             int axis, void* codes, void* scales, cudaStream_t st);
 

@@ -31,69 +31,71 @@ FA4_DEV int block_exp(float amax, float* inv) {
   return X;
 }
 
-// blocks along d: one thread per 32-element block.
+// blocks along d: one thread per 32-element block b.
+template <int FMT>
+FA4_DEV void quant_row_block(const uint4* __restrict__ x, long long b, uint8_t* __restrict__ codes,
+                             uint8_t* __restrict__ scales) {
+  uint4 v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __ldg(x + b * 4 + i);
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[i * 8 + 2 * j] = bf_lo(w[j]);
+      f[i * 8 + 2 * j + 1] = bf_hi(w[j]);
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  float inv;
+  int X = block_exp<FMT>(amax, &inv);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) f[i] *= inv;
+  scales[b] = (uint8_t)(X + 127);
+  if (FMT == 0) {
+    uint4 o;
+    o.x = pack_e2m1x8(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]);
+    o.y = pack_e2m1x8(f[8], f[9], f[10], f[11], f[12], f[13], f[14], f[15]);
+    o.z = pack_e2m1x8(f[16], f[17], f[18], f[19], f[20], f[21], f[22], f[23]);
+    o.w = pack_e2m1x8(f[24], f[25], f[26], f[27], f[28], f[29], f[30], f[31]);
+    reinterpret_cast<uint4*>(codes)[b] = o;
+  } else {
+    uint4 o0, o1;
+    o0.x = pack_e4m3x4(f[0], f[1], f[2], f[3]);
+    o0.y = pack_e4m3x4(f[4], f[5], f[6], f[7]);
+    o0.z = pack_e4m3x4(f[8], f[9], f[10], f[11]);
+    o0.w = pack_e4m3x4(f[12], f[13], f[14], f[15]);
+    o1.x = pack_e4m3x4(f[16], f[17], f[18], f[19]);
+    o1.y = pack_e4m3x4(f[20], f[21], f[22], f[23]);
+    o1.z = pack_e4m3x4(f[24], f[25], f[26], f[27]);
+    o1.w = pack_e4m3x4(f[28], f[29], f[30], f[31]);
+    reinterpret_cast<uint4*>(codes)[2 * b] = o0;
+    reinterpret_cast<uint4*>(codes)[2 * b + 1] = o1;
+  }
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict__ x,
                                                           long long nblocks,
                                                           uint8_t* __restrict__ codes,
                                                           uint8_t* __restrict__ scales) {
   for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nblocks;
-       b += (long long)gridDim.x * blockDim.x) {
-    uint4 v[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = __ldg(x + b * 4 + i);
-    float f[32];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        f[i * 8 + 2 * j] = bf_lo(w[j]);
-        f[i * 8 + 2 * j + 1] = bf_hi(w[j]);
-      }
-    }
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
-    float inv;
-    int X = block_exp<FMT>(amax, &inv);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) f[i] *= inv;
-    scales[b] = (uint8_t)(X + 127);
-    if (FMT == 0) {
-      uint4 o;
-      o.x = pack_e2m1x8(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]);
-      o.y = pack_e2m1x8(f[8], f[9], f[10], f[11], f[12], f[13], f[14], f[15]);
-      o.z = pack_e2m1x8(f[16], f[17], f[18], f[19], f[20], f[21], f[22], f[23]);
-      o.w = pack_e2m1x8(f[24], f[25], f[26], f[27], f[28], f[29], f[30], f[31]);
-      reinterpret_cast<uint4*>(codes)[b] = o;
-    } else {
-      uint4 o0, o1;
-      o0.x = pack_e4m3x4(f[0], f[1], f[2], f[3]);
-      o0.y = pack_e4m3x4(f[4], f[5], f[6], f[7]);
-      o0.z = pack_e4m3x4(f[8], f[9], f[10], f[11]);
-      o0.w = pack_e4m3x4(f[12], f[13], f[14], f[15]);
-      o1.x = pack_e4m3x4(f[16], f[17], f[18], f[19]);
-      o1.y = pack_e4m3x4(f[20], f[21], f[22], f[23]);
-      o1.z = pack_e4m3x4(f[24], f[25], f[26], f[27]);
-      o1.w = pack_e4m3x4(f[28], f[29], f[30], f[31]);
-      reinterpret_cast<uint4*>(codes)[2 * b] = o0;
-      reinterpret_cast<uint4*>(codes)[2 * b + 1] = o1;
-    }
-  }
+       b += (long long)gridDim.x * blockDim.x)
+    quant_row_block<FMT>(x, b, codes, scales);
 }
 
-// blocks along N: CTA = one (b,h) x 128-token tile, output transposed
+// blocks along N: one (b,h) x 128-token tile t0.., output transposed
 // [bh][d][Np].  Shared tile [128 tokens][d] bf16; thread (channel, 32-token
-// block) with consecutive threads on consecutive channels.
+// block) with consecutive threads on consecutive channels.  Called by the
+// whole CTA.
 template <int FMT, int D>
-__global__ void __launch_bounds__(256) quant_cols_kernel(const __nv_bfloat16* __restrict__ x,
-                                                          int N, int Np,
-                                                          uint8_t* __restrict__ codes,
-                                                          uint8_t* __restrict__ scales) {
-  __shared__ __align__(16) __nv_bfloat16 tile[128 * D];
-  const int t0 = blockIdx.x * 128;
-  const long long bh = blockIdx.y;
+FA4_DEV void quant_col_tile(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* tile, int N, int Np,
+                            int t0, long long bh, uint8_t* __restrict__ codes,
+                            uint8_t* __restrict__ scales) {
   const uint4* src = reinterpret_cast<const uint4*>(x + (bh * N + t0) * (long long)D);
   const int valid = min(128, N - t0);
   constexpr int VEC = D / 8;   // uint4 per token row
@@ -143,6 +145,41 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(const __nv_bfloat16* __
   }
 }
 
+template <int FMT, int D>
+__global__ void __launch_bounds__(256) quant_cols_kernel(const __nv_bfloat16* __restrict__ x,
+                                                          int N, int Np,
+                                                          uint8_t* __restrict__ codes,
+                                                          uint8_t* __restrict__ scales) {
+  __shared__ __align__(16) __nv_bfloat16 tile[128 * D];
+  quant_col_tile<FMT, D>(x, tile, N, Np, blockIdx.x * 128, blockIdx.y, codes, scales);
+}
+
+// Q and K (blocks along d) and V (blocks along N) in one grid.  CTA i is a V
+// tile when i is a multiple of `period` (the first nv of them), else a CTA of
+// 256 row blocks of Q, then of K: the transposes of V are spread among the row
+// streams instead of running after them.
+template <int D>
+__global__ void __launch_bounds__(256) quant_qkv_kernel(const QkvParams p) {
+  __shared__ __align__(16) __nv_bfloat16 tile[128 * D];
+  const long long i = blockIdx.x;
+  const long long P = p.period;
+  if (i % P == 0 && i / P < p.nv) {
+    const long long vt = i / P;
+    const int ntn = p.Np / 128;
+    quant_col_tile<0, D>(static_cast<const __nv_bfloat16*>(p.v), tile, p.N, p.Np, (int)(vt % ntn) * 128, vt / ntn, p.vc, p.vs);
+    return;
+  }
+  const long long before = (i + P - 1) / P;
+  const long long r = i - (before < p.nv ? before : p.nv);   // index among the row CTAs
+  if (r < p.nq_cta) {
+    const long long b = r * 256 + threadIdx.x;
+    if (b < p.nbq) quant_row_block<0>(p.q, b, p.qc, p.qs);
+  } else {
+    const long long b = (r - p.nq_cta) * 256 + threadIdx.x;
+    if (b < p.nbk) quant_row_block<0>(p.k, b, p.kc, p.ks);
+  }
+}
+
 int grid_for(long long work, int per_cta) {
   int sms = 152;
   int dev = 0;
@@ -167,6 +204,31 @@ __global__ void watchdog_selftest_kernel(unsigned* err, unsigned long long limit
 }
 
 }  // namespace
+
+cudaError_t launch_quantize_qkv(const void* q, const void* k, const void* v, long long BHq, long long BHkv,
+                                int N, int d, void* qc, void* qs, void* kc, void* ks, void* vc, void* vs,
+                                cudaStream_t st) {
+  QkvParams p;
+  p.q = (const uint4*)q;
+  p.k = (const uint4*)k;
+  p.v = v;
+  p.qc = (uint8_t*)qc; p.qs = (uint8_t*)qs;
+  p.kc = (uint8_t*)kc; p.ks = (uint8_t*)ks;
+  p.vc = (uint8_t*)vc; p.vs = (uint8_t*)vs;
+  p.N = N;
+  p.Np = padded_n(N);
+  p.nbq = BHq * N * (d / 32);
+  p.nbk = BHkv * N * (d / 32);
+  p.nq_cta = (p.nbq + 255) / 256;
+  p.nk_cta = (p.nbk + 255) / 256;
+  p.nv = (long long)(p.Np / 128) * BHkv;
+  const long long total = p.nv + p.nq_cta + p.nk_cta;
+  p.period = total / p.nv;
+  if (total > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  if (d == 128) quant_qkv_kernel<128><<<(unsigned)total, 256, 0, st>>>(p);
+  else quant_qkv_kernel<64><<<(unsigned)total, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_watchdog_selftest(unsigned* err, unsigned long long limit_ns, cudaStream_t st) {
   watchdog_selftest_kernel<<<1, 32, 0, st>>>(err, limit_ns);

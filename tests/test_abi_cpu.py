@@ -61,6 +61,14 @@ def test_argument_errors_before_launch(lib):
     assert lib.fa4fp4_fwd(*args, 1, 4, 4, 64, 64, 0.0, 0, p, 7, null, null) == INVALID # dtype
     assert lib.fa4fp4_fwd(*([p] * 5 + [odd]), 1, 4, 4, 64, 64, 0.0, 0, p, 1, null, null) == ALIGN
     assert lib.fa4bf16_fwd(null, p, p, 1, 1, 1, 64, 64, 0.0, 0, p, 1, null, null) == INVALID
+    qkv = [p] * 3
+    outs = [p] * 6
+    assert lib.fa4fp4_quantize_qkv(null, p, p, 1, 4, 2, 64, 64, *outs, null) == INVALID
+    assert lib.fa4fp4_quantize_qkv(*qkv, 1, 4, 2, 64, 64, *([p] * 5 + [null]), null) == INVALID
+    assert lib.fa4fp4_quantize_qkv(*qkv, 1, 4, 3, 64, 64, *outs, null) == UNSUP      # Hq % Hkv
+    assert lib.fa4fp4_quantize_qkv(*qkv, 1, 4, 2, 64, 96, *outs, null) == UNSUP      # d
+    assert lib.fa4fp4_quantize_qkv(p, p, odd, 1, 4, 2, 64, 64, *outs, null) == ALIGN
+    assert lib.fa4fp4_quantize_qkv(*qkv, 1, 4, 2, 64, 64, *([p] * 4 + [odd, p]), null) == ALIGN
     assert lib.fa4fp4_directp_codes(null, 10, 0.0, 1.0, 0, p, null) == INVALID
     assert lib.fa4fp4_directp_codes(p, 10, 0.0, 1.0, 2, p, null) == INVALID
     assert lib.fa4fp4_status_string(5).decode() == "device pipeline wait timed out"

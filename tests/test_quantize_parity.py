@@ -66,3 +66,32 @@ def test_full_size_q_k_v(w):
         c, s = gpu_quant(fa, x, fmt, axis)
         co, so = oracle.quantize(x.float().numpy(), fmt, axis)
         assert np.array_equal(s, so) and np.array_equal(c, co), (fmt, axis)
+
+
+@pytest.mark.parametrize("N,d", [(1, 64), (33, 128), (129, 64), (300, 128), (1000, 64)])
+def test_quantize_qkv_one_launch(N, d):
+    """The fused call writes exactly what the oracle (and three separate
+    quantize calls) give: Q and K along d, V along N, GQA head counts."""
+    fa = require_gpu()
+    g = torch.Generator().manual_seed(N + d)
+    q = torch.randn(2, 4, N, d, generator=g).to(torch.bfloat16)
+    k = (torch.randn(2, 2, N, d, generator=g) * 3).to(torch.bfloat16)
+    v = (torch.randn(2, 2, N, d, generator=g) * torch.exp2(torch.randint(-6, 6, (2, 2, N, 1), generator=g).float())).to(torch.bfloat16)
+    q4, k4, vt = fa.quantize_qkv(q.cuda(), k.cuda(), v.cuda())
+    fa.sync_status()
+    for got, x, axis in ((q4, q, 0), (k4, k, 0), (vt, v, 1)):
+        co, so = oracle.quantize(x.float().numpy(), 0, axis)
+        assert np.array_equal(got.scales.cpu().numpy(), so), axis
+        assert np.array_equal(got.codes.cpu().numpy(), co), axis
+
+
+@pytest.mark.parametrize("w", [FWD_4K, VIDEO_DIT], ids=lambda w: w.name)
+def test_quantize_qkv_full_size(w):
+    fa = require_gpu()
+    q, k, v = make_inputs(w)
+    outs = fa.quantize_qkv(q.cuda(), k.cuda(), v.cuda())
+    fa.sync_status()
+    for got, x, axis in zip(outs, (q, k, v), (0, 0, 1)):
+        co, so = oracle.quantize(x.float().numpy(), 0, axis)
+        assert np.array_equal(got.scales.cpu().numpy(), so), axis
+        assert np.array_equal(got.codes.cpu().numpy(), co), axis
