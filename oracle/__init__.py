@@ -198,7 +198,9 @@ def _rows(rows, total):
 def fwd(Q, K, V, softmax_scale: float = 0.0, causal: bool = False, mode: int = 0, rows=None):
     """Forward for selected query rows ((b*Hq+h)*N+i).  Q [B,Hq,N,d],
     K/V [B,Hkv,N,d] float arrays (dequantized values).  Returns (O [r,d],
-    LSE [r]) in float64.  mode 0 = Direct-P, mode 1 = exact exponentials."""
+    LSE [r]) in float64.  mode 0 = Direct-P, mode 1 = exact exponentials,
+    mode 2 = FP8 P/V route (P rounded through MXFP8 per 32 keys; V given as
+    the dequantized MXFP8 values)."""
     Q, K, V = _f32(Q), _f32(K), _f32(V)
     B, Hq, N, d = Q.shape
     Hkv = K.shape[1]

@@ -290,15 +290,24 @@ ORC_API void orc_directp_codes_of_x(const float* x, long n, uint8_t* out) {
  * mode 1 (textbook reduction for pins): same loop with s in FP64 and
  *   p = exp2(c*(s-m)) in place of the code value (no factor 6; LSE = scale*m +
  *   ln l).
+ * mode 2 (the FP8 P/V training route; "Stability Constraint" of the technical
+ *   summary: the retained training route keeps FP8 probabilities and values):
+ *   s and the running max as in mode 0; p = fl32(2^x), x = fmaf(s, c,
+ *   -fl32(m_j*c)); p rounded through MXFP8 (E4M3 with one E8M0 scale per 32
+ *   keys, blocks aligned to absolute key positions 32a) as the P V operand;
+ *   l <- alpha*l + sum deq(p8) (the normalizer from the same rounded values
+ *   the product consumes); O <- alpha*O + sum deq(p8)*V, V being the
+ *   dequantized MXFP8 V.  Output O/l, LSE = scale*m + ln l.
  * Causal: key n is valid for query i iff n <= i; key tiles wholly above the
  * diagonal are skipped. */
+static void mxfp8_roundtrip(double* v, int n, long stride);
 ORC_API void orc_fwd(const float* Q, const float* K, const float* V, int B, int Hq, int Hkv,
                      int N, int d, float softmax_scale, int causal, int mode, long nrows,
                      const int64_t* rows, double* O_out, double* LSE_out) {
     if (softmax_scale <= 0.0f) softmax_scale = (float)(1.0 / sqrt((double)d));
     const float c = (float)((double)softmax_scale * 1.4426950408889634);   /* fl32(scale*log2 e) */
     /* mode 1 is the real-arithmetic textbook form: c unrounded */
-    const double cr = mode == 0 ? (double)c : (double)softmax_scale * 1.4426950408889634;
+    const double cr = mode != 1 ? (double)c : (double)softmax_scale * 1.4426950408889634;
     const int group = Hq / Hkv;
     #pragma omp parallel for schedule(dynamic, 4)
     for (long r = 0; r < nrows; ++r) {
@@ -325,16 +334,26 @@ ORC_API void orc_fwd(const float* Q, const float* K, const float* V, int B, int 
                 double acc = 0.0;
                 const float* kr = Kh + (long)(j0 + n) * d;
                 for (int t = 0; t < d; ++t) acc += (double)q[t] * (double)kr[t];
-                s[n] = mode == 0 ? (double)(float)acc : acc;
+                s[n] = mode != 1 ? (double)(float)acc : acc;
                 if (s[n] > tmax) tmax = s[n];
             }
             double mnew = m > tmax ? m : tmax;
             double alpha = (m == -INFINITY) ? 1.0 : exp2(cr * (m - mnew));
             l *= alpha;
             for (int t = 0; t < d; ++t) o[t] *= alpha;
+            if (mode == 2) {
+                /* p = fl32(2^x) for the valid keys, then MXFP8 in 32-key blocks */
+                const float mc = (float)mnew * c;
+                for (int n = 0; n < cnt; ++n) s[n] = (double)(float)exp2((double)fmaf((float)s[n], c, -mc));
+                for (int a0 = 0; a0 < cnt; a0 += 32) {
+                    int nb = cnt - a0 < 32 ? cnt - a0 : 32;
+                    mxfp8_roundtrip(s + a0, nb, 1);
+                }
+            }
             for (int n = 0; n < cnt; ++n) {
                 double p;
                 if (mode == 0) p = orc_e2m1_value(orc_directp_code((float)s[n], (float)mnew, c));
+                else if (mode == 2) p = s[n];
                 else p = exp2(cr * (s[n] - mnew));
                 if (p == 0.0) continue;
                 l += p;
@@ -345,7 +364,7 @@ ORC_API void orc_fwd(const float* Q, const float* K, const float* V, int B, int 
         }
         free(s);
         for (int t = 0; t < d; ++t) o[t] /= l;
-        LSE_out[r] = (double)softmax_scale * m + log(mode == 0 ? l / 6.0 : l);
+        LSE_out[r] = (double)softmax_scale * m + log(mode == 0 ? l / 6.0 : l);   /* modes 1, 2: ln l */
     }
 }
 

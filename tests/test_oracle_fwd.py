@@ -131,25 +131,27 @@ def test_constant_v():
     assert np.all(L >= (S.max(-1).reshape(-1) / np.sqrt(d)) - 1e-9)
 
 
-def test_causal_first_row_and_future_independence():
+@pytest.mark.parametrize("mode", [0, 2])
+def test_causal_first_row_and_future_independence(mode):
     d, N = 64, 260
     Qd, Kd, Vd = quantized_inputs(rand((1, 1, N, d), 12), rand((1, 1, N, d), 13), rand((1, 1, N, d), 14))
-    O, _ = oracle.fwd(Qd, Kd, Vd, causal=True)
+    O, _ = oracle.fwd(Qd, Kd, Vd, causal=True, mode=mode)
     assert np.array_equal(O[0], Vd[0, 0, 0].astype(np.float64))
     i = 140
     K2, V2 = Kd.copy(), Vd.copy()
     K2[:, :, i + 1:] = rand((1, 1, N - i - 1, d), 15)
     V2[:, :, i + 1:] = rand((1, 1, N - i - 1, d), 16)
-    O2, _ = oracle.fwd(Qd, K2, V2, causal=True, rows=np.arange(i + 1))
+    O2, _ = oracle.fwd(Qd, K2, V2, causal=True, rows=np.arange(i + 1), mode=mode)
     assert np.array_equal(O2, O[: i + 1])
 
 
+@pytest.mark.parametrize("mode", [0, 2])
 @pytest.mark.parametrize("causal", [False, True])
-def test_gqa_equals_repeated_mha(causal):
+def test_gqa_equals_repeated_mha(causal, mode):
     d, N = 64, 200
     Qd, Kd, Vd = quantized_inputs(rand((2, 4, N, d), 17), rand((2, 2, N, d), 18), rand((2, 2, N, d), 19))
-    O, L = oracle.fwd(Qd, Kd, Vd, causal=causal)
-    Om, Lm = oracle.fwd(Qd, np.repeat(Kd, 2, 1), np.repeat(Vd, 2, 1), causal=causal)
+    O, L = oracle.fwd(Qd, Kd, Vd, causal=causal, mode=mode)
+    Om, Lm = oracle.fwd(Qd, np.repeat(Kd, 2, 1), np.repeat(Vd, 2, 1), causal=causal, mode=mode)
     assert np.array_equal(O, Om) and np.array_equal(L, Lm)
 
 
@@ -167,3 +169,81 @@ def test_directp_close_to_softmax():
     assert np.max(np.abs(L - L1)) < 0.9 and np.mean(np.abs(L - L1)) < 0.2
     cos = np.sum(O * O1, 1) / np.linalg.norm(O, axis=1) / np.linalg.norm(O1, axis=1)
     assert cos.mean() > 0.9
+
+
+# ---------------------------------------------------------------------------
+# mode 2: the FP8 P/V training route (P through MXFP8 per 32 keys)
+# ---------------------------------------------------------------------------
+
+def test_fp8pv_constant_v():
+    """The normalizer is summed from the same rounded P the product uses, so a
+    constant V row comes back unchanged (a normalizer from the unrounded p
+    would scale it by sum(p8)/sum(p))."""
+    d, N = 64, 300
+    v = np.array([0.5, -1.0, 3.0, 0.0] * (d // 4), np.float32)
+    V = np.broadcast_to(v, (1, 2, N, d)).copy()
+    Qd, Kd, _ = quantized_inputs(rand((1, 2, N, d), 30, 2.0), rand((1, 2, N, d), 31, 2.0), V)
+    O, L = oracle.fwd(Qd, Kd, V, mode=2)
+    np.testing.assert_allclose(O, np.broadcast_to(v, O.shape), rtol=0, atol=1e-12)
+    # the max key's p is 2^(rounding residual of m*c): 1 or just below it, and
+    # just below 1 the OCP rule (X = floor(log2 amax) - 8) saturates p*2^9 to
+    # 448, i.e. deq(p8) = 0.875; so l >= 0.875
+    S = np.einsum("bhid,bhjd->bhij", Qd.astype(np.float64), Kd.astype(np.float64))
+    assert np.all(L >= (S.max(-1).reshape(-1) / np.sqrt(d)) + np.log(0.875) - 1e-9)
+
+
+def test_fp8pv_equal_scores():
+    """q = 0: every score is 0, every p is exactly 1 (exact in E4M3), so O is
+    the mean of the V rows and LSE = ln N."""
+    d, N = 64, 300
+    V = rand((1, 1, N, d), 32)
+    O, L = oracle.fwd(np.zeros((1, 1, N, d), np.float32), rand((1, 1, N, d), 33), V, mode=2)
+    np.testing.assert_allclose(O, np.broadcast_to(V[0, 0].astype(np.float64).mean(0), O.shape), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(L, np.log(N), rtol=0, atol=1e-12)
+
+
+def test_fp8pv_scale_per_32_keys():
+    """Keys 0-31 have p = 1, keys 32-63 have p ~ 2^-25.5 and V ~ 2^25.5, the rest
+    p = 0.  With one E8M0 scale per 32 keys the small block keeps its own scale
+    and contributes ~1 to O[0] (O ~ 2, as exact softmax); under one scale per
+    row it would flush to 0 (O = 1)."""
+    d, N, scale = 64, 128, 0.125
+    c = np.float32(np.float32(scale) * np.float32(np.log2(np.e)))
+    Q = np.zeros((1, 1, N, d), np.float32)
+    Q[0, 0, 0, 0] = 1.0
+    K = np.zeros((1, 1, N, d), np.float32)
+    K[0, 0, 32:64, 0] = np.float32(-25.5 / float(c))
+    K[0, 0, 64:, 0] = -1000.0
+    V = np.zeros((1, 1, N, d), np.float32)
+    V[0, 0, :32, 0] = 1.0
+    V[0, 0, 32:64, 0] = np.float32(2.0 ** 25.5)
+    O2, _ = oracle.fwd(Q, K, V, softmax_scale=scale, mode=2, rows=np.arange(1))
+    O1, _ = oracle.fwd(Q, K, V, softmax_scale=scale, mode=1, rows=np.arange(1))
+    assert abs(O1[0, 0] - 2.0) < 1e-5
+    assert abs(O2[0, 0] - O1[0, 0]) < 0.05          # E4M3 rounding of 2^8.5 -> 352
+    assert abs(O2[0, 0] - 1.0) > 0.9                 # not flushed
+
+
+def test_fp8pv_permutation_within_32_key_blocks():
+    d, N = 64, 300
+    Qd, Kd, Vd = quantized_inputs(rand((1, 2, N, d), 34), rand((1, 2, N, d), 35), rand((1, 2, N, d), 36))
+    O, L = oracle.fwd(Qd, Kd, Vd, mode=2)
+    rng = np.random.default_rng(3)
+    perm = np.concatenate([rng.permutation(np.arange(t, min(N, t + 32))) for t in range(0, N, 32)])
+    Op, Lp = oracle.fwd(Qd, Kd[:, :, perm], Vd[:, :, perm], mode=2)
+    np.testing.assert_allclose(Op, O, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(Lp, L, rtol=0, atol=1e-12)
+
+
+def test_fp8pv_close_to_softmax():
+    """E4M3 P (3 mantissa bits, per-32 scales): close to exact softmax on the
+    same dequantized inputs, and closer than the E2M1 Direct-P codes."""
+    d, N = 64, 512
+    Qd, Kd, Vd = quantized_inputs(rand((1, 2, N, d), 37), rand((1, 2, N, d), 38), rand((1, 2, N, d), 39))
+    O1, L1 = oracle.fwd(Qd, Kd, Vd, mode=1)
+    O2, L2 = oracle.fwd(Qd, Kd, Vd, mode=2)
+    O0, _ = oracle.fwd(Qd, Kd, Vd, mode=0)
+    e2 = np.linalg.norm(O2 - O1) / np.linalg.norm(O1)
+    e0 = np.linalg.norm(O0 - O1) / np.linalg.norm(O1)
+    assert e2 < 0.08 and e2 < e0 / 2
+    assert np.max(np.abs(L2 - L1)) < 0.05     # a stray factor (Direct-P's 6) would be ln 6
