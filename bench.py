@@ -385,6 +385,19 @@ def run_train(fa, dev, args, world):
     fa.sync_status()
     out = {"workload": w.name, "fwd_ms": round(statistics.mean(f_ms), 4),
            "fwd_tflops": round(w.fwd_flops / (statistics.mean(f_ms) * 1e-3) / 1e12, 2)}
+
+    # the FP8 P/V training route of the forward (E4M3 P and V, MXFP8 scales)
+    v8n = fa.quantize(v, fa.FMT_MXFP8, fa.ALONG_N)
+    o8 = torch.empty_like(o)
+    lse8 = torch.empty_like(lse)
+
+    def fwd8_step(ie):
+        fa.fwd_fp8pv(q4, k4, v8n, causal=True, out_dtype=fa.OUT_F32, out=o8, lse=lse8)
+
+    f8_ms, _ = time_steps(fwd8_step, args.warmup, args.steps, flush, world)
+    fa.sync_status()
+    out["fwd_fp8pv_ms"] = round(statistics.mean(f8_ms), 4)
+    out["fwd_fp8pv_tflops"] = round(w.fwd_flops / (statistics.mean(f8_ms) * 1e-3) / 1e12, 2)
     ws = torch.empty(max(fa.bwd_workspace_bytes(B, Hq, Hkv, N, d), 16), dtype=torch.uint8, device=dev)
     try:
         fa.bwd(q4, k4, q8c, k8c, v8r, o, do, lse, causal=True, workspace=ws)

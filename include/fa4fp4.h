@@ -112,6 +112,23 @@ FA4FP4_API fa4fp4_status fa4fp4_fwd(const void* q_codes, const void* q_scales, c
                          int B, int Hq, int Hkv, int N, int d, float softmax_scale, int causal,
                          void* o, int out_dtype, float* lse, void* stream);
 
+/* The FP8 P/V training route of the forward (technical summary, Methodology 2
+ * "Stability Constraint" and Training Performance: the retained training route
+ * keeps FP8 probabilities and values).  Same arguments, layouts and errors as
+ * fa4fp4_fwd except V: v8_codes/v8_scales is V quantized to MXFP8 with blocks
+ * along N (fa4fp4_quantize with FA4FP4_FMT_MXFP8_E4M3, FA4FP4_BLOCKS_ALONG_N:
+ * E4M3 codes [B][Hkv][d][Np], scales [B][Hkv][d][Np/32]).  Per 128-key tile
+ * in ascending order: S = Q K^T on FP4 tensor cores, running max m, p =
+ * 2^x with x = fl32(fl32(s - m) c) in FP32 (hardware exponential; the row max
+ * gets p = 1 exactly), P rounded to E4M3
+ * with one E8M0 scale per 32 keys (OCP MX rule), O += P V and l += P 1 on
+ * FP8 tensor cores (kind::mxf8f6f4), eager rescale when m grows.  Outputs
+ * O / l and LSE = softmax_scale * m + ln(l). */
+FA4FP4_API fa4fp4_status fa4fp4_fwd_fp8pv(const void* q_codes, const void* q_scales, const void* k_codes,
+                                          const void* k_scales, const void* v8_codes, const void* v8_scales,
+                                          int B, int Hq, int Hkv, int N, int d, float softmax_scale, int causal,
+                                          void* o, int out_dtype, float* lse, void* stream);
+
 /* Bytes of caller-provided workspace fa4fp4_bwd needs. */
 FA4FP4_API size_t fa4fp4_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
 

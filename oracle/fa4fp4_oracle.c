@@ -292,8 +292,11 @@ ORC_API void orc_directp_codes_of_x(const float* x, long n, uint8_t* out) {
  *   ln l).
  * mode 2 (the FP8 P/V training route; "Stability Constraint" of the technical
  *   summary: the retained training route keeps FP8 probabilities and values):
- *   s and the running max as in mode 0; p = fl32(2^x), x = fmaf(s, c,
- *   -fl32(m_j*c)); p rounded through MXFP8 (E4M3 with one E8M0 scale per 32
+ *   s and the running max as in mode 0; p = fl32(2^x) with x =
+ *   fl32(fl32(s - m_j) * c) (the difference first: it is exact near the max,
+ *   so the row max gets x = 0 and p = 1 exactly, never the value just below
+ *   1 that the E4M3 block rule would saturate); p rounded through MXFP8
+ *   (E4M3 with one E8M0 scale per 32
  *   keys, blocks aligned to absolute key positions 32a) as the P V operand;
  *   l <- alpha*l + sum deq(p8) (the normalizer from the same rounded values
  *   the product consumes); O <- alpha*O + sum deq(p8)*V, V being the
@@ -342,9 +345,13 @@ ORC_API void orc_fwd(const float* Q, const float* K, const float* V, int B, int 
             l *= alpha;
             for (int t = 0; t < d; ++t) o[t] *= alpha;
             if (mode == 2) {
-                /* p = fl32(2^x) for the valid keys, then MXFP8 in 32-key blocks */
-                const float mc = (float)mnew * c;
-                for (int n = 0; n < cnt; ++n) s[n] = (double)(float)exp2((double)fmaf((float)s[n], c, -mc));
+                /* p = fl32(2^x), x = fl32(fl32(s - m) * c), for the valid keys,
+                 * then MXFP8 in 32-key blocks */
+                for (int n = 0; n < cnt; ++n) {
+                    const float dx = (float)s[n] - (float)mnew;
+                    const float x = dx * c;
+                    s[n] = (double)(float)exp2((double)x);
+                }
                 for (int a0 = 0; a0 < cnt; a0 += 32) {
                     int nb = cnt - a0 < 32 ? cnt - a0 : 32;
                     mxfp8_roundtrip(s + a0, nb, 1);

@@ -52,6 +52,8 @@ def load_library():
         lib.fa4fp4_quantize.argtypes = [vp, i, i, i, i, i, i, vp, vp, vp]
         lib.fa4fp4_quantize_qkv.restype = i
         lib.fa4fp4_quantize_qkv.argtypes = [vp, vp, vp, i, i, i, i, i] + [vp] * 7
+        lib.fa4fp4_fwd_fp8pv.restype = i
+        lib.fa4fp4_fwd_fp8pv.argtypes = [vp] * 6 + [i, i, i, i, i, f, i, vp, i, vp, vp]
         lib.fa4fp4_fwd.restype = i
         lib.fa4fp4_fwd.argtypes = [vp] * 6 + [i, i, i, i, i, f, i, vp, i, vp, vp]
         lib.fa4fp4_bwd_workspace_bytes.restype = sz
@@ -165,6 +167,27 @@ def fwd(q: QTensor, k: QTensor, vt: QTensor, causal: bool = False, softmax_scale
     _cuda(q.codes, q.scales, k.codes, k.scales, vt.codes, vt.scales, out, lse)
     _check("fa4fp4_fwd", load_library().fa4fp4_fwd(
         _ptr(q.codes), _ptr(q.scales), _ptr(k.codes), _ptr(k.scales), _ptr(vt.codes), _ptr(vt.scales),
+        B, Hq, Hkv, N, d, float(softmax_scale), int(bool(causal)), _ptr(out), out_dtype,
+        _ptr(lse) if with_lse else None, _stream(dev)))
+    return out, (lse if with_lse else None)
+
+
+def fwd_fp8pv(q: QTensor, k: QTensor, v8t: QTensor, causal: bool = False, softmax_scale: float = 0.0,
+              out_dtype: int = OUT_BF16, with_lse: bool = True, out=None, lse=None):
+    """FP8 P/V route of the forward (fa4fp4_fwd_fp8pv): MXFP4 Q/K, V as MXFP8
+    blocked along N.  Returns (o, lse or None)."""
+    if v8t.fmt != FMT_MXFP8 or v8t.axis != ALONG_N:
+        raise ValueError("fwd_fp8pv expects V quantized to MXFP8 with blocks along N")
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    dev = q.codes.device
+    if out is None:
+        out = torch.empty((B, Hq, N, d), dtype=torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32, device=dev)
+    if with_lse and lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    _cuda(q.codes, q.scales, k.codes, k.scales, v8t.codes, v8t.scales, out, lse)
+    _check("fa4fp4_fwd_fp8pv", load_library().fa4fp4_fwd_fp8pv(
+        _ptr(q.codes), _ptr(q.scales), _ptr(k.codes), _ptr(k.scales), _ptr(v8t.codes), _ptr(v8t.scales),
         B, Hq, Hkv, N, d, float(softmax_scale), int(bool(causal)), _ptr(out), out_dtype,
         _ptr(lse) if with_lse else None, _stream(dev)))
     return out, (lse if with_lse else None)

@@ -158,10 +158,12 @@ fa4fp4_status fa4fp4_quantize_qkv(const void* q, const void* k, const void* v, i
                                            static_cast<cudaStream_t>(stream)));
 }
 
-fa4fp4_status fa4fp4_fwd(const void* qc, const void* qs, const void* kc, const void* ks,
-                         const void* vc, const void* vs, int B, int Hq, int Hkv, int N, int d,
-                         float softmax_scale, int causal, void* o, int out_dtype, float* lse,
-                         void* stream) {
+// Shared by the Direct-P forward (fp8pv = 0, V^T MXFP4) and the FP8 P/V
+// route (fp8pv = 1, V^T MXFP8).
+static fa4fp4_status fwd_common(const void* qc, const void* qs, const void* kc, const void* ks,
+                                const void* vc, const void* vs, int B, int Hq, int Hkv, int N, int d,
+                                float softmax_scale, int causal, void* o, int out_dtype, float* lse,
+                                int fp8pv, void* stream) {
   if (!qc || !qs || !kc || !ks || !vc || !vs || !o) return FA4FP4_ERR_INVALID_ARG;
   if (out_dtype != FA4FP4_OUT_F32 && out_dtype != FA4FP4_OUT_BF16) return FA4FP4_ERR_INVALID_ARG;
   fa4fp4_status s = check_dims(B, Hq, Hkv, N, d);
@@ -175,10 +177,13 @@ fa4fp4_status fa4fp4_fwd(const void* qc, const void* qs, const void* kc, const v
   memset(&p, 0, sizeof(p));
   const int Np = padded_n(N);
   const CUtensorMapSwizzle qsw = d == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  // V^T rows of 128 keys: 64 bytes of E2M1 (64-byte swizzle) or 128 bytes of
+  // E4M3 (128-byte swizzle)
+  const int vrow = fp8pv ? 128 : 64;
   if (!make_map(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qc, d / 2, N, (uint64_t)B * Hq, d / 2, 128, qsw) ||
       !make_map(&p.tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kc, d / 2, N, (uint64_t)B * Hkv, d / 2, 128, qsw) ||
-      !make_map(&p.tm_v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, vc, Np / 2, d, (uint64_t)B * Hkv, 64, d,
-                CU_TENSOR_MAP_SWIZZLE_64B))
+      !make_map(&p.tm_v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, vc, fp8pv ? Np : Np / 2, d, (uint64_t)B * Hkv, vrow, d,
+                fp8pv ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
     return FA4FP4_ERR_CUDA;
   p.q_scales = static_cast<const uint8_t*>(qs);
   p.k_scales = static_cast<const uint8_t*>(ks);
@@ -190,11 +195,28 @@ fa4fp4_status fa4fp4_fwd(const void* qc, const void* qs, const void* kc, const v
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.Np = Np;
   p.causal = causal ? 1 : 0;
   p.out_bf16 = out_dtype == FA4FP4_OUT_BF16;
+  p.fp8pv = fp8pv;
   p.scale = default_scale(softmax_scale, d);
   p.c = (float)((double)p.scale * 1.4426950408889634);
   const float* T = directp_thresholds();
   for (int k = 0; k < 7; ++k) p.T[k] = T[k];
   return launch_status(launch_fwd_fp4(p, static_cast<cudaStream_t>(stream)));
+}
+
+fa4fp4_status fa4fp4_fwd(const void* qc, const void* qs, const void* kc, const void* ks,
+                         const void* vc, const void* vs, int B, int Hq, int Hkv, int N, int d,
+                         float softmax_scale, int causal, void* o, int out_dtype, float* lse,
+                         void* stream) {
+  return fwd_common(qc, qs, kc, ks, vc, vs, B, Hq, Hkv, N, d, softmax_scale, causal, o, out_dtype, lse,
+                    0, stream);
+}
+
+fa4fp4_status fa4fp4_fwd_fp8pv(const void* qc, const void* qs, const void* kc, const void* ks,
+                               const void* v8c, const void* v8s, int B, int Hq, int Hkv, int N, int d,
+                               float softmax_scale, int causal, void* o, int out_dtype, float* lse,
+                               void* stream) {
+  return fwd_common(qc, qs, kc, ks, v8c, v8s, B, Hq, Hkv, N, d, softmax_scale, causal, o, out_dtype, lse,
+                    1, stream);
 }
 
 fa4fp4_status fa4fp4_directp_codes(const float* s, int64_t n, float m, float c, int native_exp,

@@ -36,34 +36,42 @@ namespace {
 
 constexpr int BM = 128;         // queries per tile; a CTA holds two tiles
 constexpr int BN = 128;         // keys per tile
-constexpr int STAGES = 6;       // K/V pipeline depth
 constexpr int NSOFT = 8;        // softmax warps: 4 per query tile
 constexpr int NTHREADS = 32 * (2 + NSOFT);
 constexpr uint32_t TMEM_COLS = 512;
-// S at 0, O_X at 128 + 128X, l_X at 384 + 16X, scale factors from 416
-constexpr uint32_t COL_S = 0, COL_O0 = 128, COL_L0 = 384, COL_SFQ0 = 416, COL_SFP = 424,
-                   COL_SFK = 428, COL_SFV = 428 + 4 * STAGES;
-static_assert(COL_SFV + 4 * STAGES <= TMEM_COLS, "TMEM budget");
+constexpr uint32_t COL_S = 0, COL_O0 = 128, COL_L0 = 384;   // O_X at 128 + 128X, l_X at 384 + 16X
 
-template <int D>
-struct Smem {
-  static constexpr int QB = BM * D / 2;   // bytes of a Q or K code tile
+// Shared-memory and TMEM layout of one CTA.  P8: the FP8 P/V route (E4M3 P
+// and V^T, one E8M0 scale per 32 keys), else Direct-P (E2M1 P and V^T).
+template <int D, bool P8>
+struct Layout {
+  static constexpr int STAGES = P8 ? 4 : 6;   // K/V pipeline depth
+  static constexpr int QB = BM * D / 2;       // bytes of a Q or K code tile
   static constexpr int KB = BN * D / 2;
-  static constexpr int VB = D * BN / 2;   // V^T: D rows of 128 keys
-  static constexpr int PB = BM * BN / 2;
-  static constexpr int ONESB = 16 * 64;   // 16 rows of 128 E2M1 ones
+  static constexpr int PROW = P8 ? BN : BN / 2;   // bytes of a P (or V^T) row of 128 keys
+  static constexpr int VB = D * PROW;         // V^T: D rows of 128 keys
+  static constexpr int PB = BM * PROW;
+  static constexpr int ONESB = 16 * PROW;     // 16 rows of 128 ones
   static constexpr int OFF_Q = 0;                          // Q_A, Q_B
   static constexpr int OFF_K = OFF_Q + 2 * QB;
   static constexpr int OFF_V = OFF_K + STAGES * KB;
   static constexpr int OFF_P = OFF_V + STAGES * VB;        // [tile X][2 buffers]
   static constexpr int OFF_ONES = OFF_P + 4 * PB;
   static constexpr int OFF_SF = OFF_ONES + ONESB;         // 512-byte scale chunks
-  static constexpr int SF_Q = OFF_SF, SF_P = SF_Q + 1024, SF_K = SF_P + 512,
-                       SF_V = SF_K + 512 * STAGES;
+  static constexpr int SF_Q = OFF_SF;                     // [X]
+  static constexpr int SF_1 = SF_Q + 1024;                // unit scales (ones tile; Direct-P P)
+  static constexpr int SF_P = SF_1 + 512;                 // P8: [X][step parity]
+  static constexpr int SF_K = SF_P + (P8 ? 4 * 512 : 0);
+  static constexpr int SF_V = SF_K + 512 * STAGES;
   static constexpr int OFF_BAR = SF_V + 512 * STAGES;
   static constexpr int NBAR = 1 + 4 * STAGES + 2 + 2 + 2 + 2 + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int BYTES = OFF_MISC + 64 + 1024;    // + alignment slack
+  // TMEM scale-factor columns (4 each): Q_X, unit, P_X (P8), K and V rings
+  static constexpr uint32_t COL_SFQ0 = 416, COL_SF1 = 424, COL_SFP0 = 428,
+                            COL_SFK = 428 + (P8 ? 8 : 0), COL_SFV = COL_SFK + 4 * STAGES;
+  static_assert(COL_SFV + 4 * STAGES <= TMEM_COLS, "TMEM budget");
+  static_assert(BYTES <= 227 * 1024, "shared memory budget");
 };
 
 // Direct-P code of one scaled offset x: #{k : x >= T_k}.
@@ -147,9 +155,12 @@ FA4_DEV void stage_sf_rows(uint8_t* chunk, const uint8_t* src, int row0, int nro
   *reinterpret_cast<uint4*>(chunk + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-template <int D>
+template <int D, bool P8>
 __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_constant__ FwdFp4Params p) {
-  using L = Smem<D>;
+  using L = Layout<D, P8>;
+  constexpr int STAGES = L::STAGES;
+  constexpr uint32_t COL_SFQ0 = L::COL_SFQ0, COL_SF1 = L::COL_SF1, COL_SFP0 = L::COL_SFP0,
+                     COL_SFK = L::COL_SFK, COL_SFV = L::COL_SFV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
@@ -196,11 +207,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
     fence_barrier_init();
   }
   if (warp == 1) {
-    // unit E8M0 scale (byte 127) for every P block and the ones tile; the
-    // ones tile holds E2M1 1.0 (code 2) in every nibble
-    reinterpret_cast<uint4*>(smem + L::SF_P)[lane] = make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
-    reinterpret_cast<uint4*>(smem + L::OFF_ONES)[lane] = make_uint4(0x22222222u, 0x22222222u, 0x22222222u, 0x22222222u);
-    reinterpret_cast<uint4*>(smem + L::OFF_ONES)[lane + 32] = make_uint4(0x22222222u, 0x22222222u, 0x22222222u, 0x22222222u);
+    // unit E8M0 scale (byte 127) for the ones tile (and every Direct-P P
+    // block); the ones tile holds 1.0 in every element: E2M1 code 2 per nibble
+    // or E4M3 code 0x38 per byte
+    reinterpret_cast<uint4*>(smem + L::SF_1)[lane] = make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
+    const uint32_t one = P8 ? 0x38383838u : 0x22222222u;
+#pragma unroll
+    for (int i = 0; i < L::ONESB / 512; ++i)
+      reinterpret_cast<uint4*>(smem + L::OFF_ONES)[lane + 32 * i] = make_uint4(one, one, one, one);
     fence_proxy_async_smem();
     tmem_alloc(tmem_holder, TMEM_COLS);
   }
@@ -266,7 +280,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(&v_full[st], L::VB);
-        tma_load_3d(smem + L::OFF_V + st * L::VB, &p.tm_v, &v_full[st], j * (BN / 2), 0, bkv);
+        tma_load_3d(smem + L::OFF_V + st * L::VB, &p.tm_v, &v_full[st], j * L::PROW, 0, bkv);
       }
       issued = j + 1;
     }
@@ -284,8 +298,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
     const bool leader = elect_one();
     constexpr int KSTEPS = D / 64;   // K = 64 per mxf4 MMA
     const uint32_t idesc_s = idesc_bs(BM, BN, 1, 1, false, false, 0, 0);
-    const uint32_t idesc_o = idesc_bs(BM, D, 1, 1, false, false, 0, 0);
-    const uint32_t idesc_l = idesc_bs(BM, 16, 1, 1, false, false, 0, 0);
+    // P V and the normalizer: E2M1 (kind::mxf4 code 1) or E4M3 (kind::mxf8f6f4 code 0)
+    const uint32_t idesc_o = idesc_bs(BM, D, P8 ? 0 : 1, P8 ? 0 : 1, false, false, 0, 0);
+    const uint32_t idesc_l = idesc_bs(BM, 16, P8 ? 0 : 1, P8 ? 0 : 1, false, false, 0, 0);
     constexpr Swizzle QSW = D == 128 ? SW_64B : SW_32B;
     constexpr uint32_t QSBO = D == 128 ? 512 : 256;
     const uint32_t sq = smem_u32(smem + L::OFF_Q);
@@ -295,7 +310,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
     if (ok && leader) {
       tmem_cp_sf(tbase + COL_SFQ0, smem + L::SF_Q);
       tmem_cp_sf(tbase + COL_SFQ0 + 4, smem + L::SF_Q + 512);
-      tmem_cp_sf(tbase + COL_SFP, smem + L::SF_P);
+      tmem_cp_sf(tbase + COL_SF1, smem + L::SF_1);
     }
     __syncwarp();
     // S = Q_X K_t^T once the other tile's warps hold their S (first = no wait)
@@ -341,14 +356,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       const uint32_t sp = smem_u32(smem + L::OFF_P + (2 * x + (t & 1)) * L::PB);
       const uint32_t sv = smem_u32(smem + L::OFF_V + st * L::VB);
       if (leader) {
+        if constexpr (P8) {
+          // E4M3 P with its per-32-key scales (this tile, this step)
+          tmem_cp_sf(tbase + COL_SFP0 + 4 * x, smem + L::SF_P + (2 * x + (t & 1)) * 512);
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {     // 128 keys = 2 x K64
-          const uint64_t ad = make_sdesc(sp + 32 * k, 16, 512, SW_64B);
-          const uint32_t sf = ((uint32_t)(2 * k) << 29) | ((uint32_t)(2 * k) << 4);
-          mma_mxf4(tbase + COL_O0 + 128 * x, ad, make_sdesc(sv + 32 * k, 16, 512, SW_64B), idesc_o | sf,
-                   tbase + COL_SFP, tbase + COL_SFV + 4 * st, t > 0 || k > 0);
-          mma_mxf4(tbase + COL_L0 + 16 * x, ad, make_sdesc(sones + 32 * k, 16, 512, SW_64B), idesc_l | sf,
-                   tbase + COL_SFP, tbase + COL_SFP, t > 0 || k > 0);
+          for (int k = 0; k < 4; ++k) {   // 128 keys = 4 x K32
+            const uint64_t ad = make_sdesc(sp + 32 * k, 16, 1024, SW_128B);
+            const uint32_t sf = ((uint32_t)k << 29) | ((uint32_t)k << 4);
+            mma_mxf8(tbase + COL_O0 + 128 * x, ad, make_sdesc(sv + 32 * k, 16, 1024, SW_128B), idesc_o | sf,
+                     tbase + COL_SFP0 + 4 * x, tbase + COL_SFV + 4 * st, t > 0 || k > 0);
+            mma_mxf8(tbase + COL_L0 + 16 * x, ad, make_sdesc(sones + 32 * k, 16, 1024, SW_128B), idesc_l | sf,
+                     tbase + COL_SFP0 + 4 * x, tbase + COL_SF1, t > 0 || k > 0);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {   // 128 keys = 2 x K64
+            const uint64_t ad = make_sdesc(sp + 32 * k, 16, 512, SW_64B);
+            const uint32_t sf = ((uint32_t)(2 * k) << 29) | ((uint32_t)(2 * k) << 4);
+            mma_mxf4(tbase + COL_O0 + 128 * x, ad, make_sdesc(sv + 32 * k, 16, 512, SW_64B), idesc_o | sf,
+                     tbase + COL_SF1, tbase + COL_SFV + 4 * st, t > 0 || k > 0);
+            mma_mxf4(tbase + COL_L0 + 16 * x, ad, make_sdesc(sones + 32 * k, 16, 512, SW_64B), idesc_l | sf,
+                     tbase + COL_SF1, tbase + COL_SF1, t > 0 || k > 0);
+          }
         }
         mma_commit(&o_done[x]);
         if (x == 1) mma_commit(&v_empty[st]);
@@ -384,8 +413,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
     const float c = p.c;
     const float (&T)[7] = p.T;                // read from the parameter space
     const int lim = p.causal ? min(p.N - 1, qi) : p.N - 1;   // last key of the row
-    const int sw = (r >> 1) & 3;              // 64-byte swizzle phase of row r
-    uint8_t* prow = smem + L::OFF_P + 2 * x * L::PB + r * 64;
+    // swizzle phase of row r: 64-byte rows (E2M1) or 128-byte rows (E4M3)
+    const int sw = P8 ? (r & 7) : ((r >> 1) & 3);
+    uint8_t* prow = smem + L::OFF_P + 2 * x * L::PB + r * L::PROW;
     float m = -INFINITY;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
@@ -417,11 +447,42 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       const float m_new = fmaxf(m, max128(s));
       const float mc = m_new * c;
       uint8_t* pb = prow + (j & 1) * L::PB;
+      if constexpr (P8) {
+        // p = 2^x with x = fl32(fl32(s - m) * c) (exact difference near the
+        // max: the row max gets p = 1 exactly), then E4M3 with one E8M0 scale
+        // per 32 keys (OCP MX rule: X = E(amax) - 127 - 8); the row's four
+        // scale bytes go to the scale-factor chunk of this tile and step
+        uint32_t sfw = 0;
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        uint32_t pw[4];
-        directp_codes32(s[g], c, mc, T, pw);
-        *reinterpret_cast<uint4*>(pb + ((g ^ sw) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+        for (int g = 0; g < 4; ++g) {
+          float amax = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float2 xx = fmul2(fadd2(make_float2(s[g][i], s[g][i + 1]), make_float2(-m_new, -m_new)),
+                                    make_float2(c, c));
+            s[g][i] = ex2_approx(xx.x);
+            s[g][i + 1] = ex2_approx(xx.y);
+            amax = fmax3(amax, s[g][i], s[g][i + 1]);
+          }
+          int X = (int)((__float_as_uint(amax) >> 23) & 0xff) - 127 - 8;
+          X = X < -127 ? -127 : (X > 127 ? 127 : X);
+          const float inv = __uint_as_float((uint32_t)(127 - X) << 23);
+          sfw |= (uint32_t)(X + 127) << (8 * g);
+          uint32_t w[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            w[e] = pack_e4m3x4(s[g][4 * e] * inv, s[g][4 * e + 1] * inv, s[g][4 * e + 2] * inv, s[g][4 * e + 3] * inv);
+          *reinterpret_cast<uint4*>(pb + (((2 * g) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(pb + (((2 * g + 1) ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+        *reinterpret_cast<uint32_t*>(smem + L::SF_P + (2 * x + (j & 1)) * 512 + (r % 32) * 16 + (r / 32) * 4) = sfw;
+      } else {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t pw[4];
+          directp_codes32(s[g], c, mc, T, pw);
+          *reinterpret_cast<uint4*>(pb + ((g ^ sw) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+        }
       }
       fence_proxy_async_smem();
       if (j > 0) {
@@ -490,7 +551,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
                                  __uint_as_float(v[4 * q + 2]) * inv_l, __uint_as_float(v[4 * q + 3]) * inv_l);
         }
       }
-      if (valid && p.lse) p.lse[(long long)bh * p.N + qi] = p.scale * m + logf(l * (1.f / 6.f));
+      // LSE: Direct-P codes carry the factor 6 of 6*2^x, the FP8 route does not
+      if (valid && p.lse) p.lse[(long long)bh * p.N + qi] = p.scale * m + logf(P8 ? l : l * (1.f / 6.f));
     }
   }
   tc_fence_before();
@@ -543,19 +605,20 @@ __global__ void directp_codes_kernel(const float* __restrict__ s, long long n, f
 
 }  // namespace
 
-cudaError_t launch_fwd_fp4(const FwdFp4Params& p, cudaStream_t st) {
+template <int D, bool P8>
+static cudaError_t launch_fwd_t(const FwdFp4Params& p, cudaStream_t st) {
+  using L = Layout<D, P8>;
   const int nq = (p.N + BM - 1) / BM;
   dim3 grid((nq + 1) / 2, p.B * p.Hq);
-  if (p.d == 128) {
-    auto k = fwd_fp4_kernel<128>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<128>::BYTES);
-    k<<<grid, NTHREADS, Smem<128>::BYTES, st>>>(p);
-  } else {
-    auto k = fwd_fp4_kernel<64>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<64>::BYTES);
-    k<<<grid, NTHREADS, Smem<64>::BYTES, st>>>(p);
-  }
+  auto k = fwd_fp4_kernel<D, P8>;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
+  k<<<grid, NTHREADS, L::BYTES, st>>>(p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_fp4(const FwdFp4Params& p, cudaStream_t st) {
+  if (p.fp8pv) return p.d == 128 ? launch_fwd_t<128, true>(p, st) : launch_fwd_t<64, true>(p, st);
+  return p.d == 128 ? launch_fwd_t<128, false>(p, st) : launch_fwd_t<64, false>(p, st);
 }
 
 cudaError_t launch_directp_codes(const float* s, long long n, float m, float c, const float* T,

@@ -34,7 +34,8 @@ cudaError_t launch_quantize(const void* x, long long rows, int d, int N, long lo
 
 // ---------------------------------------------------------------- FP4 fwd
 struct FwdFp4Params {
-  CUtensorMap tm_q, tm_k, tm_v;     // MXFP4 codes of Q, K (along d) and V^T (along N)
+  CUtensorMap tm_q, tm_k, tm_v;     // MXFP4 codes of Q, K (along d); V^T (along N): MXFP4,
+                                    // or MXFP8 for the FP8 P/V route
   const uint8_t* q_scales;
   const uint8_t* k_scales;
   const uint8_t* v_scales;
@@ -42,6 +43,7 @@ struct FwdFp4Params {
   float* lse;
   unsigned* err;
   int B, Hq, Hkv, N, d, Np, causal, out_bf16;
+  int fp8pv;                        // 0: Direct-P (E2M1 P); 1: FP8 P/V route (E4M3 P and V)
   float scale, c;                   // softmax scale, fl32(scale*log2 e)
   float T[7];                       // Direct-P thresholds
 };

@@ -185,11 +185,9 @@ def test_fp8pv_constant_v():
     Qd, Kd, _ = quantized_inputs(rand((1, 2, N, d), 30, 2.0), rand((1, 2, N, d), 31, 2.0), V)
     O, L = oracle.fwd(Qd, Kd, V, mode=2)
     np.testing.assert_allclose(O, np.broadcast_to(v, O.shape), rtol=0, atol=1e-12)
-    # the max key's p is 2^(rounding residual of m*c): 1 or just below it, and
-    # just below 1 the OCP rule (X = floor(log2 amax) - 8) saturates p*2^9 to
-    # 448, i.e. deq(p8) = 0.875; so l >= 0.875
+    # the max key has x = 0, p = 1, exact in E4M3 under its block scale: l >= 1
     S = np.einsum("bhid,bhjd->bhij", Qd.astype(np.float64), Kd.astype(np.float64))
-    assert np.all(L >= (S.max(-1).reshape(-1) / np.sqrt(d)) + np.log(0.875) - 1e-9)
+    assert np.all(L >= (S.max(-1).reshape(-1) / np.sqrt(d)) - 1e-9)
 
 
 def test_fp8pv_equal_scores():
