@@ -156,6 +156,35 @@ def dequantize(codes, scales, shape, fmt: int, axis: int) -> np.ndarray:
     return out
 
 
+def nvfp4_tensor_scale(x) -> float:
+    x = _f32(x)
+    _load().orc_nvfp4_tensor_scale.restype = ctypes.c_float
+    return float(_load().orc_nvfp4_tensor_scale(_ptr(x, ctypes.c_float), ctypes.c_long(x.size)))
+
+
+def quantize_nvfp4(x):
+    """NVFP4 along d: returns (codes [B,H,N,d/2], scales [B,H,N,d/16] E4M3
+    bytes, tensor scale float)."""
+    x = _f32(x)
+    B, H, N, d = x.shape
+    ts = nvfp4_tensor_scale(x)
+    codes = np.zeros((B, H, N, d // 2), dtype=np.uint8)
+    scales = np.zeros((B, H, N, d // 16), dtype=np.uint8)
+    _load().orc_quantize_nvfp4(_ptr(x, ctypes.c_float), B, H, N, d, ctypes.c_float(ts),
+                               _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8))
+    return codes, scales, ts
+
+
+def dequantize_nvfp4(codes, scales, ts, shape) -> np.ndarray:
+    B, H, N, d = shape
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    out = np.zeros((B, H, N, d), dtype=np.float32)
+    _load().orc_dequantize_nvfp4(_ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8),
+                                 ctypes.c_float(ts), B, H, N, d, _ptr(out, ctypes.c_float))
+    return out
+
+
 # --------------------------------------------------------------------------
 # Direct-P
 # --------------------------------------------------------------------------

@@ -186,6 +186,70 @@ ORC_API void orc_dequantize(const uint8_t* codes, const uint8_t* scales, int B, 
 }
 
 /* ------------------------------------------------------------------------ */
+/* NVFP4 (Methodology 1, "Format Selection": NVFP4 for Q and K, for its      */
+/* fine-grained scaling)                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* The pages name NVFP4 but give no rule.  Reading: the public NVFP4 format,
+ * E2M1 elements with one unsigned E4M3 scale per 16 consecutive elements along
+ * d and one FP32 scale per tensor, every step an FP32 operation rounded to
+ * nearest:
+ *   amax_t = max |x| over the tensor; ts = amax_t / 2688 (2688 = 6 * 448: the
+ *   tensor's largest block then takes the largest E2M1 value under the
+ *   largest E4M3 scale); ts = 1 for an all-zero tensor;
+ *   per block of 16: sb = E4M3(amax_b / (6 * ts)) (RNE, saturating);
+ *   each element: code = E2M1(x / (sb * ts)) (RNE, saturating, sign kept); a
+ *   block whose scale rounds to zero gets signed-zero codes.
+ * A value dequantizes to e2m1(code) * sb * ts. */
+ORC_API float orc_nvfp4_tensor_scale(const float* x, long n) {
+    float amax = 0.0f;
+    for (long i = 0; i < n; ++i) if (fabsf(x[i]) > amax) amax = fabsf(x[i]);
+    return amax > 0.0f ? amax / 2688.0f : 1.0f;
+}
+
+/* x logical [B,H,N,d] FP32 (bf16 values); codes [B,H,N,d/2] (element 2i in
+ * the low nibble), scales [B,H,N,d/16] E4M3 bytes, ts from
+ * orc_nvfp4_tensor_scale of the same tensor. */
+ORC_API void orc_quantize_nvfp4(const float* x, int B, int H, int N, int d, float ts, uint8_t* codes,
+                                uint8_t* scales) {
+    long rows = (long)B * H * N;
+    int nb = d / 16;
+    const float six_ts = 6.0f * ts;
+    #pragma omp parallel for schedule(static)
+    for (long r = 0; r < rows; ++r) {
+        for (int blk = 0; blk < nb; ++blk) {
+            const float* v = x + r * d + blk * 16;
+            float amax = 0.0f;
+            for (int t = 0; t < 16; ++t) if (fabsf(v[t]) > amax) amax = fabsf(v[t]);
+            const float sbf = amax / six_ts;
+            const int sbc = orc_round_to_code((double)sbf, 1);
+            scales[r * nb + blk] = (uint8_t)sbc;
+            const float den = (float)orc_e4m3_value(sbc) * ts;
+            for (int t = 0; t < 16; ++t) {
+                int code;
+                if (den == 0.0f) code = signbit(v[t]) ? 0x8 : 0x0;
+                else code = orc_round_to_code((double)(v[t] / den), 0);
+                long e = r * d + blk * 16 + t;
+                uint8_t* byte = &codes[e / 2];
+                if ((e & 1) == 0) *byte = (uint8_t)((*byte & 0xf0) | code);
+                else *byte = (uint8_t)((*byte & 0x0f) | (code << 4));
+            }
+        }
+    }
+}
+
+ORC_API void orc_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales, float ts, int B, int H,
+                                  int N, int d, float* out) {
+    long n = (long)B * H * N * d;
+    #pragma omp parallel for schedule(static)
+    for (long e = 0; e < n; ++e) {
+        int code = (codes[e / 2] >> (4 * (e & 1))) & 0xf;
+        double sb = orc_e4m3_value(scales[e / 16]);
+        out[e] = (float)(orc_e2m1_value(code) * sb * (double)ts);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Direct-P (Methodology 1, "Direct Mapping")                                */
 /* ------------------------------------------------------------------------ */
 

@@ -169,3 +169,53 @@ def test_nibble_order():
     codes, scales = oracle.quantize(x, 0, oracle.ALONG_D)
     assert scales[0, 0, 0, 0] == 127
     assert codes[0, 0, 0, 0] == (0x6 | (0x1 << 4))
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 (E2M1, one E4M3 scale per 16 along d, one FP32 scale per tensor)
+# ---------------------------------------------------------------------------
+
+def nvfp4_reference(x):
+    """The reading's steps in numpy FP32 with the independent round-half-even
+    helpers above: ts = amax/2688; sb = RNE_E4M3(amax_b / (6 ts));
+    y = x / (sb ts); RNE_E2M1(y) * sb * ts."""
+    x = np.asarray(x, np.float32)
+    amax = np.float32(np.abs(x).max())
+    ts = np.float32(amax / np.float32(2688.0)) if amax > 0 else np.float32(1.0)
+    blocks = x.reshape(-1, 16)
+    ab = np.abs(blocks).max(1).astype(np.float32)
+    sb = rne_e4m3((ab / np.float32(np.float32(6.0) * ts)).astype(np.float64)).astype(np.float32)
+    den = (sb * ts).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = (blocks / den[:, None]).astype(np.float32)
+    q = np.where(den[:, None] == 0, 0.0, rne_e2m1(y.astype(np.float64)))
+    return (q * sb[:, None].astype(np.float64) * np.float64(ts)).reshape(x.shape), sb, ts
+
+
+def test_nvfp4_matches_independent_steps():
+    g = np.random.default_rng(4)
+    x = g.standard_normal((2, 3, 50, 64)) * np.exp2(g.integers(-10, 10, (2, 3, 50, 4)).repeat(16, -1))
+    x = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    x[0, 0, 0, :16] = 0.0                      # an all-zero block: scale 0, codes 0
+    codes, scales, ts = oracle.quantize_nvfp4(x)
+    want, sb, ts_ref = nvfp4_reference(x)
+    assert np.float32(ts) == ts_ref
+    assert np.array_equal(np.array([oracle.e4m3_value(int(c)) for c in scales.reshape(-1)]), sb.astype(np.float64))
+    got = oracle.dequantize_nvfp4(codes, scales, ts, x.shape)      # FP32 values
+    assert np.array_equal(got, want.astype(np.float32))
+    assert scales.reshape(-1)[0] == 0 and np.all(codes[0, 0, 0, :8] == 0)
+
+
+def test_nvfp4_invariants():
+    g = torch.Generator().manual_seed(9)
+    x = torch.randn(1, 2, 33, 128, generator=g).to(torch.bfloat16).float().numpy()
+    c0, s0, t0 = oracle.quantize_nvfp4(x)
+    for k in (-7, 3):
+        c1, s1, t1 = oracle.quantize_nvfp4(np.ldexp(x, k).astype(np.float32))
+        assert np.array_equal(c1, c0) and np.array_equal(s1, s0) and t1 == np.ldexp(t0, k)
+    cn, sn, tn = oracle.quantize_nvfp4(-x)
+    assert np.array_equal(cn, c0 ^ 0x88) and np.array_equal(sn, s0) and tn == t0
+    # the largest element lands on the top of the grid: 6 * 448 * ts = amax
+    deq = oracle.dequantize_nvfp4(c0, s0, t0, x.shape)
+    i = np.unravel_index(np.abs(x).argmax(), x.shape)
+    assert abs(deq[i] - x[i]) <= abs(x[i]) * 2.0 ** -3
