@@ -219,3 +219,20 @@ def test_nvfp4_invariants():
     deq = oracle.dequantize_nvfp4(c0, s0, t0, x.shape)
     i = np.unravel_index(np.abs(x).argmax(), x.shape)
     assert abs(deq[i] - x[i]) <= abs(x[i]) * 2.0 ** -3
+
+
+def test_nvfp4_grid_tops():
+    """Properties that fix the two constants: in every block the largest
+    element lands on the top of the E2M1 grid (6, within the E4M3 rounding of
+    the block scale: 2^-4 relative for normal scales), and the tensor's
+    largest block carries the largest E4M3 scale (448)."""
+    g = np.random.default_rng(12)
+    x = g.standard_normal((1, 2, 64, 128)) * np.exp2(g.integers(-5, 5, (1, 2, 64, 8)).repeat(16, -1))
+    x = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    codes, scales, ts = oracle.quantize_nvfp4(x)
+    sb = np.array([oracle.e4m3_value(int(c)) for c in scales.reshape(-1)])
+    amax_b = np.abs(x.reshape(-1, 16)).max(1).astype(np.float64)
+    normal = sb >= 2.0 ** -6
+    top = amax_b[normal] / (sb[normal] * ts)
+    assert np.all(top >= 6 / (1 + 2.0 ** -4) - 1e-9) and np.all(top <= 6 / (1 - 2.0 ** -4) + 1e-9)
+    assert sb[np.argmax(amax_b)] == 448.0 and sb.max() == 448.0
