@@ -358,8 +358,16 @@ def run_workloads(fa, dev, steps):
         b_ms, _ = time_steps(lambda ie: fa.bf16_fwd(q, k, v, out=o, lse=lse), 2, steps, flush, 1)
         fa.sync_status()
         fm, bm = statistics.mean(f_ms), statistics.mean(b_ms)
-        out.append({"workload": w.name, "fp4_tflops": round(w.fwd_flops / (fm * 1e-3) / 1e12, 1),
-                    "bf16_tflops": round(w.fwd_flops / (bm * 1e-3) / 1e12, 1), "speedup": round(bm / fm, 3)})
+        row = {"workload": w.name, "fp4_tflops": round(w.fwd_flops / (fm * 1e-3) / 1e12, 1),
+               "bf16_tflops": round(w.fwd_flops / (bm * 1e-3) / 1e12, 1), "speedup": round(bm / fm, 3)}
+        if w is VIDEO_DIT:
+            # NVFP4 Q/K (the pages' Q/K format) on the outlier-channel workload
+            qn, kn = fa.quantize_nvfp4(q), fa.quantize_nvfp4(k)
+            n_ms, _ = time_steps(lambda ie: fa.fwd_nvfp4(qn, kn, vt, out=o, lse=lse), 2, steps, flush, 1)
+            fa.sync_status()
+            row["fp4_nvfp4_qk_tflops"] = round(w.fwd_flops / (statistics.mean(n_ms) * 1e-3) / 1e12, 1)
+            del qn, kn
+        out.append(row)
         del q, k, v, q4, k4, vt, o, lse
         torch.cuda.empty_cache()
     return out

@@ -129,6 +129,32 @@ FA4FP4_API fa4fp4_status fa4fp4_fwd_fp8pv(const void* q_codes, const void* q_sca
                                           int B, int Hq, int Hkv, int N, int d, float softmax_scale, int causal,
                                           void* o, int out_dtype, float* lse, void* stream);
 
+/* NVFP4 block quantization along d (technical summary, Methodology 1
+ * "Format Selection": NVFP4 for Q and K, for its fine-grained scaling; the
+ * public NVFP4 layout).  x_bf16 is [B][H][N][d] bf16.  Writes codes
+ * [B][H][N][d/2] (E2M1, element 2i in the low nibble), scales [B][H][N][d/16]
+ * (unsigned E4M3, one per 16 elements) and *ts, the tensor's FP32 scale, in
+ * device memory.  Every step is an FP32 operation rounded to nearest: ts =
+ * amax/2688 (1 for an all-zero tensor), block scale E4M3(amax_b / (6 ts)),
+ * element E2M1(x / (block scale * ts)), saturating, sign kept; a block whose
+ * scale rounds to zero gets signed zeros.  Three launches on `stream` (tensor
+ * amax, tensor scale, blocks); *ts is also their scratch word. */
+FA4FP4_API fa4fp4_status fa4fp4_quantize_nvfp4(const void* x_bf16, int B, int H, int N, int d, void* codes,
+                                               void* scales, float* ts, void* stream);
+
+/* The forward with NVFP4 Q and K (from fa4fp4_quantize_nvfp4): q_ts and k_ts
+ * point to their device tensor scales.  S = Q K^T runs as tcgen05 kind::mxf4nvf4
+ * (UE4M3 scales per 16); the two tensor scales fold into the softmax scale,
+ * fl32(fl32(softmax_scale * q_ts) * k_ts), which also enters the LSE.  fp8pv
+ * selects the P/V path: 0 = Direct-P with V^T as MXFP4 (fa4fp4_fwd), 1 = the
+ * FP8 P/V route with V^T as MXFP8 (fa4fp4_fwd_fp8pv).  Other arguments and
+ * errors as fa4fp4_fwd. */
+FA4FP4_API fa4fp4_status fa4fp4_fwd_nvfp4(const void* q_codes, const void* q_scales, const float* q_ts,
+                                          const void* k_codes, const void* k_scales, const float* k_ts,
+                                          const void* vt_codes, const void* vt_scales, int B, int Hq, int Hkv,
+                                          int N, int d, float softmax_scale, int causal, int fp8pv, void* o,
+                                          int out_dtype, float* lse, void* stream);
+
 /* Bytes of caller-provided workspace fa4fp4_bwd needs. */
 FA4FP4_API size_t fa4fp4_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
 

@@ -54,6 +54,10 @@ def load_library():
         lib.fa4fp4_quantize_qkv.argtypes = [vp, vp, vp, i, i, i, i, i] + [vp] * 7
         lib.fa4fp4_fwd_fp8pv.restype = i
         lib.fa4fp4_fwd_fp8pv.argtypes = [vp] * 6 + [i, i, i, i, i, f, i, vp, i, vp, vp]
+        lib.fa4fp4_quantize_nvfp4.restype = i
+        lib.fa4fp4_quantize_nvfp4.argtypes = [vp, i, i, i, i, vp, vp, vp, vp]
+        lib.fa4fp4_fwd_nvfp4.restype = i
+        lib.fa4fp4_fwd_nvfp4.argtypes = [vp] * 8 + [i, i, i, i, i, f, i, i, vp, i, vp, vp]
         lib.fa4fp4_fwd.restype = i
         lib.fa4fp4_fwd.argtypes = [vp] * 6 + [i, i, i, i, i, f, i, vp, i, vp, vp]
         lib.fa4fp4_bwd_workspace_bytes.restype = sz
@@ -190,6 +194,53 @@ def fwd_fp8pv(q: QTensor, k: QTensor, v8t: QTensor, causal: bool = False, softma
         _ptr(q.codes), _ptr(q.scales), _ptr(k.codes), _ptr(k.scales), _ptr(v8t.codes), _ptr(v8t.scales),
         B, Hq, Hkv, N, d, float(softmax_scale), int(bool(causal)), _ptr(out), out_dtype,
         _ptr(lse) if with_lse else None, _stream(dev)))
+    return out, (lse if with_lse else None)
+
+
+@dataclass
+class NvTensor:
+    """NVFP4 tensor: E2M1 codes [B,H,N,d/2], E4M3 scales [B,H,N,d/16], and the
+    FP32 tensor scale in a one-element device tensor."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+    ts: torch.Tensor
+    shape: tuple
+
+
+def quantize_nvfp4(x: torch.Tensor, out: NvTensor | None = None) -> NvTensor:
+    """NVFP4 along d of a bf16 [B,H,N,d] CUDA tensor (fa4fp4_quantize_nvfp4)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 4:
+        raise ValueError("quantize_nvfp4 expects a bf16 [B,H,N,d] tensor")
+    _cuda(x)
+    B, H, N, d = x.shape
+    if out is None:
+        out = NvTensor(torch.empty((B, H, N, d // 2), dtype=torch.uint8, device=x.device),
+                       torch.empty((B, H, N, d // 16), dtype=torch.uint8, device=x.device),
+                       torch.empty(1, dtype=torch.float32, device=x.device), (B, H, N, d))
+    _check("fa4fp4_quantize_nvfp4", load_library().fa4fp4_quantize_nvfp4(
+        _ptr(x), B, H, N, d, _ptr(out.codes), _ptr(out.scales), _ptr(out.ts), _stream(x.device)))
+    return out
+
+
+def fwd_nvfp4(q: NvTensor, k: NvTensor, vt: QTensor, causal: bool = False, softmax_scale: float = 0.0,
+              out_dtype: int = OUT_BF16, with_lse: bool = True, out=None, lse=None):
+    """Forward with NVFP4 Q/K (fa4fp4_fwd_nvfp4).  vt MXFP4 along N gives
+    Direct-P, MXFP8 along N the FP8 P/V route.  Returns (o, lse or None)."""
+    if vt.axis != ALONG_N:
+        raise ValueError("fwd_nvfp4 expects V blocked along N")
+    fp8pv = 1 if vt.fmt == FMT_MXFP8 else 0
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    dev = q.codes.device
+    if out is None:
+        out = torch.empty((B, Hq, N, d), dtype=torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32, device=dev)
+    if with_lse and lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    _cuda(q.codes, q.scales, q.ts, k.codes, k.scales, k.ts, vt.codes, vt.scales, out, lse)
+    _check("fa4fp4_fwd_nvfp4", load_library().fa4fp4_fwd_nvfp4(
+        _ptr(q.codes), _ptr(q.scales), _ptr(q.ts), _ptr(k.codes), _ptr(k.scales), _ptr(k.ts),
+        _ptr(vt.codes), _ptr(vt.scales), B, Hq, Hkv, N, d, float(softmax_scale), int(bool(causal)), fp8pv,
+        _ptr(out), out_dtype, _ptr(lse) if with_lse else None, _stream(dev)))
     return out, (lse if with_lse else None)
 
 

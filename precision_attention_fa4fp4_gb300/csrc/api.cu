@@ -163,8 +163,11 @@ fa4fp4_status fa4fp4_quantize_qkv(const void* q, const void* k, const void* v, i
 static fa4fp4_status fwd_common(const void* qc, const void* qs, const void* kc, const void* ks,
                                 const void* vc, const void* vs, int B, int Hq, int Hkv, int N, int d,
                                 float softmax_scale, int causal, void* o, int out_dtype, float* lse,
-                                int fp8pv, void* stream) {
+                                int fp8pv, const float* ts_q, const float* ts_k, void* stream) {
   if (!qc || !qs || !kc || !ks || !vc || !vs || !o) return FA4FP4_ERR_INVALID_ARG;
+  if ((ts_q == nullptr) != (ts_k == nullptr)) return FA4FP4_ERR_INVALID_ARG;
+  if ((ts_q && (reinterpret_cast<uintptr_t>(ts_q) & 3)) || (ts_k && (reinterpret_cast<uintptr_t>(ts_k) & 3)))
+    return FA4FP4_ERR_ALIGNMENT;
   if (out_dtype != FA4FP4_OUT_F32 && out_dtype != FA4FP4_OUT_BF16) return FA4FP4_ERR_INVALID_ARG;
   fa4fp4_status s = check_dims(B, Hq, Hkv, N, d);
   if (s != FA4FP4_OK) return s;
@@ -196,6 +199,8 @@ static fa4fp4_status fwd_common(const void* qc, const void* qs, const void* kc, 
   p.causal = causal ? 1 : 0;
   p.out_bf16 = out_dtype == FA4FP4_OUT_BF16;
   p.fp8pv = fp8pv;
+  p.ts_q = ts_q;
+  p.ts_k = ts_k;
   p.scale = default_scale(softmax_scale, d);
   p.c = (float)((double)p.scale * 1.4426950408889634);
   const float* T = directp_thresholds();
@@ -208,7 +213,7 @@ fa4fp4_status fa4fp4_fwd(const void* qc, const void* qs, const void* kc, const v
                          float softmax_scale, int causal, void* o, int out_dtype, float* lse,
                          void* stream) {
   return fwd_common(qc, qs, kc, ks, vc, vs, B, Hq, Hkv, N, d, softmax_scale, causal, o, out_dtype, lse,
-                    0, stream);
+                    0, nullptr, nullptr, stream);
 }
 
 fa4fp4_status fa4fp4_fwd_fp8pv(const void* qc, const void* qs, const void* kc, const void* ks,
@@ -216,7 +221,28 @@ fa4fp4_status fa4fp4_fwd_fp8pv(const void* qc, const void* qs, const void* kc, c
                                float softmax_scale, int causal, void* o, int out_dtype, float* lse,
                                void* stream) {
   return fwd_common(qc, qs, kc, ks, v8c, v8s, B, Hq, Hkv, N, d, softmax_scale, causal, o, out_dtype, lse,
-                    1, stream);
+                    1, nullptr, nullptr, stream);
+}
+
+fa4fp4_status fa4fp4_fwd_nvfp4(const void* qc, const void* qs, const float* q_ts, const void* kc,
+                               const void* ks, const float* k_ts, const void* vc, const void* vs, int B,
+                               int Hq, int Hkv, int N, int d, float softmax_scale, int causal, int fp8pv,
+                               void* o, int out_dtype, float* lse, void* stream) {
+  if (!q_ts || !k_ts || (fp8pv != 0 && fp8pv != 1)) return FA4FP4_ERR_INVALID_ARG;
+  return fwd_common(qc, qs, kc, ks, vc, vs, B, Hq, Hkv, N, d, softmax_scale, causal, o, out_dtype, lse,
+                    fp8pv, q_ts, k_ts, stream);
+}
+
+fa4fp4_status fa4fp4_quantize_nvfp4(const void* x, int B, int H, int N, int d, void* codes, void* scales,
+                                    float* ts, void* stream) {
+  if (!x || !codes || !scales || !ts) return FA4FP4_ERR_INVALID_ARG;
+  fa4fp4_status s = check_dims(B, H, H, N, d);
+  if (s != FA4FP4_OK && !(H == 0 && s == FA4FP4_ERR_UNSUPPORTED)) return s;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || (reinterpret_cast<uintptr_t>(ts) & 3))
+    return FA4FP4_ERR_ALIGNMENT;
+  if (B == 0 || H == 0) return FA4FP4_OK;
+  return launch_status(launch_quantize_nvfp4(x, (long long)B * H * N * d, codes, scales, ts,
+                                             static_cast<cudaStream_t>(stream)));
 }
 
 fa4fp4_status fa4fp4_directp_codes(const float* s, int64_t n, float m, float c, int native_exp,

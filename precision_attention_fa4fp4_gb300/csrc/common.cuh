@@ -259,6 +259,18 @@ FA4_DEV void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t 
       : "memory");
 }
 
+// kind::mxf4nvf4 with one UE4M3 scale per 16 elements of K (4 per K=64 MMA);
+// the instruction descriptor's scale-format bit (23) is 0 for UE4M3.
+FA4_DEV void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                      uint32_t sfa_tmem, uint32_t sfb_tmem, bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
 FA4_DEV void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                       uint32_t sfa_tmem, uint32_t sfb_tmem, bool accumulate) {
   asm volatile(

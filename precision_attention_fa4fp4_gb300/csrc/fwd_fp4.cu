@@ -43,8 +43,12 @@ constexpr uint32_t COL_S = 0, COL_O0 = 128, COL_L0 = 384;   // O_X at 128 + 128X
 
 // Shared-memory and TMEM layout of one CTA.  P8: the FP8 P/V route (E4M3 P
 // and V^T, one E8M0 scale per 32 keys), else Direct-P (E2M1 P and V^T).
-template <int D, bool P8>
+// NV: NVFP4 Q and K (one UE4M3 scale per 16 along d: d/64 scale chunks per
+// tile, one per K=64 MMA step), else MXFP4 (one E8M0 scale per 32: one chunk).
+template <int D, bool P8, bool NV>
 struct Layout {
+  static constexpr int QSB = NV ? D / 16 : D / 32;   // scale bytes per Q/K row
+  static constexpr int NSC = NV ? D / 64 : 1;        // scale chunks per Q/K tile
   static constexpr int STAGES = P8 ? 4 : 6;   // K/V pipeline depth
   static constexpr int QB = BM * D / 2;       // bytes of a Q or K code tile
   static constexpr int KB = BN * D / 2;
@@ -58,18 +62,18 @@ struct Layout {
   static constexpr int OFF_P = OFF_V + STAGES * VB;        // [tile X][2 buffers]
   static constexpr int OFF_ONES = OFF_P + 4 * PB;
   static constexpr int OFF_SF = OFF_ONES + ONESB;         // 512-byte scale chunks
-  static constexpr int SF_Q = OFF_SF;                     // [X]
-  static constexpr int SF_1 = SF_Q + 1024;                // unit scales (ones tile; Direct-P P)
+  static constexpr int SF_Q = OFF_SF;                     // [X][NSC]
+  static constexpr int SF_1 = SF_Q + 2 * NSC * 512;       // unit scales (ones tile; Direct-P P)
   static constexpr int SF_P = SF_1 + 512;                 // P8: [X][step parity]
-  static constexpr int SF_K = SF_P + (P8 ? 4 * 512 : 0);
-  static constexpr int SF_V = SF_K + 512 * STAGES;
+  static constexpr int SF_K = SF_P + (P8 ? 4 * 512 : 0);  // [stage][NSC]
+  static constexpr int SF_V = SF_K + 512 * NSC * STAGES;
   static constexpr int OFF_BAR = SF_V + 512 * STAGES;
   static constexpr int NBAR = 1 + 4 * STAGES + 2 + 2 + 2 + 2 + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int BYTES = OFF_MISC + 64 + 1024;    // + alignment slack
-  // TMEM scale-factor columns (4 each): Q_X, unit, P_X (P8), K and V rings
-  static constexpr uint32_t COL_SFQ0 = 416, COL_SF1 = 424, COL_SFP0 = 428,
-                            COL_SFK = 428 + (P8 ? 8 : 0), COL_SFV = COL_SFK + 4 * STAGES;
+  // TMEM scale-factor columns (4 per chunk): Q_X, unit, P_X (P8), K and V rings
+  static constexpr uint32_t COL_SFQ0 = 416, COL_SF1 = COL_SFQ0 + 8 * NSC, COL_SFP0 = COL_SF1 + 4,
+                            COL_SFK = COL_SFP0 + (P8 ? 8 : 0), COL_SFV = COL_SFK + 4 * NSC * STAGES;
   static_assert(COL_SFV + 4 * STAGES <= TMEM_COLS, "TMEM budget");
   static_assert(BYTES <= 227 * 1024, "shared memory budget");
 };
@@ -137,17 +141,19 @@ FA4_DEV float max128(const float (&s)[4][32]) {
 }
 
 // Rearrange 128 rows of per-row scale words into the scale-factor chunk:
-// chunk byte (r%32)*16 + (r/32)*4 + kblock.  Called by a full warp.
+// chunk byte (r%32)*16 + (r/32)*4 + kblock.  The word of row r is the 4 (or,
+// for 2-byte rows, 2) scale bytes at byte `off` of the row.  Called by a full
+// warp.
 FA4_DEV void stage_sf_rows(uint8_t* chunk, const uint8_t* src, int row0, int nrows_valid,
-                           int bytes_per_row, int lane) {
+                           int bytes_per_row, int lane, int off = 0) {
   uint32_t w[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     int r = lane + 32 * c;
     uint32_t v = 0;
     if (r < nrows_valid) {
-      const uint8_t* p = src + (long long)(row0 + r) * bytes_per_row;
-      v = bytes_per_row == 4 ? *reinterpret_cast<const uint32_t*>(p)
+      const uint8_t* p = src + (long long)(row0 + r) * bytes_per_row + off;
+      v = bytes_per_row >= 4 ? *reinterpret_cast<const uint32_t*>(p)
                              : (uint32_t)*reinterpret_cast<const uint16_t*>(p);
     }
     w[c] = v;
@@ -155,9 +161,10 @@ FA4_DEV void stage_sf_rows(uint8_t* chunk, const uint8_t* src, int row0, int nro
   *reinterpret_cast<uint4*>(chunk + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-template <int D, bool P8>
+template <int D, bool P8, bool NV>
 __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_constant__ FwdFp4Params p) {
-  using L = Layout<D, P8>;
+  using L = Layout<D, P8, NV>;
+  constexpr int NSC = L::NSC, QSB = L::QSB;
   constexpr int STAGES = L::STAGES;
   constexpr uint32_t COL_SFQ0 = L::COL_SFQ0, COL_SF1 = L::COL_SF1, COL_SFP0 = L::COL_SFP0,
                      COL_SFK = L::COL_SFK, COL_SFV = L::COL_SFV;
@@ -230,9 +237,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
     }
-    const uint8_t* qs = p.q_scales + (long long)bh * p.N * (D / 32);
-    stage_sf_rows(smem + L::SF_Q, qs, q0, min(BM, p.N - q0), D / 32, lane);
-    stage_sf_rows(smem + L::SF_Q + 512, qs, q0 + BM, min(BM, p.N - q0 - BM), D / 32, lane);
+    const uint8_t* qs = p.q_scales + (long long)bh * p.N * QSB;
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+#pragma unroll
+      for (int k = 0; k < NSC; ++k)
+        stage_sf_rows(smem + L::SF_Q + (x * NSC + k) * 512, qs, q0 + x * BM, min(BM, p.N - q0 - x * BM), QSB,
+                      lane, 4 * k);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
@@ -240,7 +251,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       tma_load_3d(smem + L::OFF_Q, &p.tm_q, q_full, 0, q0, bh);
       tma_load_3d(smem + L::OFF_Q + L::QB, &p.tm_q, q_full, 0, q0 + BM, bh);
     }
-    const uint8_t* ks = p.k_scales + (long long)bkv * p.N * (D / 32);
+    const uint8_t* ks = p.k_scales + (long long)bkv * p.N * QSB;
     const uint8_t* vs = p.v_scales + (long long)bkv * D * (p.Np / 32);
     int issued = 0;
     for (int j = 0; j < nt; ++j) {
@@ -249,17 +260,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       // K_j: codes by TMA, scales rearranged into the chunk (cp.async for
       // 4-byte scale words, plain loads for the 2-byte words of d = 64)
       if (j >= STAGES && !mbar_wait(&k_empty[st], ph, abort_flag, p.err)) break;
-      uint8_t* kchunk = smem + L::SF_K + 512 * st;
-      if (D == 128) {
+      uint8_t* kchunk = smem + L::SF_K + 512 * NSC * st;
+      if (QSB >= 4) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int r = lane + 32 * c;
-          const bool in = j * BN + r < p.N;
-          cp_async4(kchunk + lane * 16 + 4 * c, ks + (long long)(j * BN + (in ? r : 0)) * 4, in ? 4u : 0u);
-        }
+        for (int k = 0; k < NSC; ++k)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int r = lane + 32 * c;
+            const bool in = j * BN + r < p.N;
+            cp_async4(kchunk + 512 * k + lane * 16 + 4 * c, ks + (long long)(j * BN + (in ? r : 0)) * QSB + 4 * k,
+                      in ? 4u : 0u);
+          }
         cp_async_mbar_arrive(&k_full[st]);
       } else {
-        stage_sf_rows(kchunk, ks, j * BN, min(BN, p.N - j * BN), D / 32, lane);
+        stage_sf_rows(kchunk, ks, j * BN, min(BN, p.N - j * BN), QSB, lane);
         fence_proxy_async_smem();
       }
       __syncwarp();
@@ -308,8 +322,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
     bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
     tc_fence_after();
     if (ok && leader) {
-      tmem_cp_sf(tbase + COL_SFQ0, smem + L::SF_Q);
-      tmem_cp_sf(tbase + COL_SFQ0 + 4, smem + L::SF_Q + 512);
+#pragma unroll
+      for (int i = 0; i < 2 * NSC; ++i) tmem_cp_sf(tbase + COL_SFQ0 + 4 * i, smem + L::SF_Q + 512 * i);
       tmem_cp_sf(tbase + COL_SF1, smem + L::SF_1);
     }
     __syncwarp();
@@ -320,7 +334,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
         if (!mbar_wait(&k_full[st], (t / STAGES) & 1, abort_flag, p.err)) return false;
         fence_proxy_async_smem();
         tc_fence_after();
-        if (leader) tmem_cp_sf(tbase + COL_SFK + 4 * st, smem + L::SF_K + 512 * st);
+        if (leader) {
+#pragma unroll
+          for (int k = 0; k < NSC; ++k)
+            tmem_cp_sf(tbase + COL_SFK + 4 * (NSC * st + k), smem + L::SF_K + 512 * (NSC * st + k));
+        }
         __syncwarp();
       }
       // the S buffer's last reader: tile B of t-1 (for A), tile A of t (for B)
@@ -333,8 +351,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
         for (int k = 0; k < KSTEPS; ++k) {
           uint64_t ad = make_sdesc(sqx + 32 * k, 16, QSBO, QSW);
           uint64_t bd = make_sdesc(sk + 32 * k, 16, QSBO, QSW);
-          uint32_t id = idesc_s | ((uint32_t)(2 * k) << 29) | ((uint32_t)(2 * k) << 4);
-          mma_mxf4(tbase + COL_S, ad, bd, id, tbase + COL_SFQ0 + 4 * x, tbase + COL_SFK + 4 * st, k > 0);
+          if constexpr (NV) {
+            // UE4M3 scales (descriptor bit 23 clear), chunk k holds the 4
+            // scales of this K=64 step
+            mma_nvf4(tbase + COL_S, ad, bd, idesc_s & ~(1u << 23), tbase + COL_SFQ0 + 4 * (x * NSC + k),
+                     tbase + COL_SFK + 4 * (NSC * st + k), k > 0);
+          } else {
+            uint32_t id = idesc_s | ((uint32_t)(2 * k) << 29) | ((uint32_t)(2 * k) << 4);
+            mma_mxf4(tbase + COL_S, ad, bd, id, tbase + COL_SFQ0 + 4 * x, tbase + COL_SFK + 4 * st, k > 0);
+          }
         }
         mma_commit(&s_full[x]);
         if (x == 1) mma_commit(&k_empty[st]);
@@ -410,7 +435,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
     const int r = quad * 32 + lane;           // row within the tile
     const int qi = q0 + x * BM + r;
     const uint32_t lane_base = tbase + ((uint32_t)(quad * 32) << 16);
-    const float c = p.c;
+    // NVFP4 Q/K: the MMA's scores lack the two tensor scales, which fold into
+    // the softmax scale: fl32(fl32(scale * ts_q) * ts_k)
+    float c = p.c, sm_scale = p.scale;
+    if constexpr (NV) {
+      sm_scale = (p.scale * *p.ts_q) * *p.ts_k;
+      c = (float)((double)sm_scale * 1.4426950408889634);
+    }
     const float (&T)[7] = p.T;                // read from the parameter space
     const int lim = p.causal ? min(p.N - 1, qi) : p.N - 1;   // last key of the row
     // swizzle phase of row r: 64-byte rows (E2M1) or 128-byte rows (E4M3)
@@ -552,7 +583,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
         }
       }
       // LSE: Direct-P codes carry the factor 6 of 6*2^x, the FP8 route does not
-      if (valid && p.lse) p.lse[(long long)bh * p.N + qi] = p.scale * m + logf(P8 ? l : l * (1.f / 6.f));
+      if (valid && p.lse) p.lse[(long long)bh * p.N + qi] = sm_scale * m + logf(P8 ? l : l * (1.f / 6.f));
     }
   }
   tc_fence_before();
@@ -605,20 +636,25 @@ __global__ void directp_codes_kernel(const float* __restrict__ s, long long n, f
 
 }  // namespace
 
-template <int D, bool P8>
+template <int D, bool P8, bool NV>
 static cudaError_t launch_fwd_t(const FwdFp4Params& p, cudaStream_t st) {
-  using L = Layout<D, P8>;
+  using L = Layout<D, P8, NV>;
   const int nq = (p.N + BM - 1) / BM;
   dim3 grid((nq + 1) / 2, p.B * p.Hq);
-  auto k = fwd_fp4_kernel<D, P8>;
+  auto k = fwd_fp4_kernel<D, P8, NV>;
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
   k<<<grid, NTHREADS, L::BYTES, st>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_fp4(const FwdFp4Params& p, cudaStream_t st) {
-  if (p.fp8pv) return p.d == 128 ? launch_fwd_t<128, true>(p, st) : launch_fwd_t<64, true>(p, st);
-  return p.d == 128 ? launch_fwd_t<128, false>(p, st) : launch_fwd_t<64, false>(p, st);
+  const bool nv = p.ts_q != nullptr;
+  if (p.fp8pv) {
+    if (nv) return p.d == 128 ? launch_fwd_t<128, true, true>(p, st) : launch_fwd_t<64, true, true>(p, st);
+    return p.d == 128 ? launch_fwd_t<128, true, false>(p, st) : launch_fwd_t<64, true, false>(p, st);
+  }
+  if (nv) return p.d == 128 ? launch_fwd_t<128, false, true>(p, st) : launch_fwd_t<64, false, true>(p, st);
+  return p.d == 128 ? launch_fwd_t<128, false, false>(p, st) : launch_fwd_t<64, false, false>(p, st);
 }
 
 cudaError_t launch_directp_codes(const float* s, long long n, float m, float c, const float* T,

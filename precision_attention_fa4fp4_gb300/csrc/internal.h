@@ -29,6 +29,10 @@ struct QkvParams {
 cudaError_t launch_quantize_qkv(const void* q, const void* k, const void* v, long long BHq, long long BHkv,
                                 int N, int d, void* qc, void* qs, void* kc, void* ks, void* vc, void* vs,
                                 cudaStream_t st);
+// NVFP4 along d of n bf16 values (n a multiple of 16): codes, E4M3 scales per
+// 16, the FP32 tensor scale into *ts (device).
+cudaError_t launch_quantize_nvfp4(const void* x, long long n, void* codes, void* scales, float* ts,
+                                  cudaStream_t st);
 cudaError_t launch_quantize(const void* x, long long rows, int d, int N, long long BH, int fmt,
                             int axis, void* codes, void* scales, cudaStream_t st);
 
@@ -44,6 +48,8 @@ struct FwdFp4Params {
   unsigned* err;
   int B, Hq, Hkv, N, d, Np, causal, out_bf16;
   int fp8pv;                        // 0: Direct-P (E2M1 P); 1: FP8 P/V route (E4M3 P and V)
+  const float* ts_q;                // NVFP4 Q/K: device tensor scales; nullptr for MXFP4 Q/K
+  const float* ts_k;
   float scale, c;                   // softmax scale, fl32(scale*log2 e)
   float T[7];                       // Direct-P thresholds
 };

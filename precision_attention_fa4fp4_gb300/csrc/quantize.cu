@@ -11,6 +11,7 @@
 // per block for blocks along d, and a shared-memory transpose of 128-token
 // tiles for blocks along N.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include "common.cuh"
 #include "internal.h"
 
@@ -180,6 +181,83 @@ __global__ void __launch_bounds__(256) quant_qkv_kernel(const QkvParams p) {
   }
 }
 
+// ---------------------------------------------------------------- NVFP4
+// E2M1 elements, one unsigned E4M3 scale per 16 consecutive elements along d,
+// one FP32 scale per tensor ("Format Selection": NVFP4 for Q and K).  Every
+// step is an FP32 operation rounded to nearest: ts = amax_t / 2688, block
+// scale sb = E4M3(amax_b / (6 ts)), element code E2M1(x / (sb ts)); a block
+// whose scale rounds to zero gets signed-zero codes.
+
+// max |x| of the tensor into *amax_bits (non-negative floats order as their
+// bit patterns); the caller zeroes it first
+__global__ void __launch_bounds__(256) nvfp4_amax_kernel(const uint4* __restrict__ x, long long nvec,
+                                                         unsigned* __restrict__ amax_bits) {
+  float m = 0.f;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nvec;
+       i += (long long)gridDim.x * blockDim.x) {
+    const uint4 v = __ldg(x + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = fmax3(m, fabsf(bf_lo(w[j])), fabsf(bf_hi(w[j])));
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if ((threadIdx.x & 31) == 0 && m > 0.f) atomicMax(amax_bits, __float_as_uint(m));
+}
+
+// the tensor's amax (bits, in place) -> its scale
+__global__ void nvfp4_tensor_scale_kernel(float* ts) {
+  const float amax = __uint_as_float(*reinterpret_cast<unsigned*>(ts));
+  *ts = amax > 0.f ? amax / 2688.0f : 1.0f;
+}
+
+FA4_DEV float e4m3_byte_value(uint32_t b) {
+  uint32_t h;
+  asm("{\n .reg .b16 t;\n mov.b16 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}\n" : "=r"(h) : "h"((unsigned short)b));
+  return __half2float(__ushort_as_half((unsigned short)(h & 0xffffu)));
+}
+
+// one thread per 16-element block
+__global__ void __launch_bounds__(256) quant_nvfp4_kernel(const uint4* __restrict__ x, long long nblocks,
+                                                          const float* __restrict__ tsp,
+                                                          uint8_t* __restrict__ codes,
+                                                          uint8_t* __restrict__ scales) {
+  const float ts = *tsp;
+  const float six_ts = 6.0f * ts;
+  for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nblocks;
+       b += (long long)gridDim.x * blockDim.x) {
+    const uint4 v0 = __ldg(x + 2 * b), v1 = __ldg(x + 2 * b + 1);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float f[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      f[2 * j] = bf_lo(w[j]);
+      f[2 * j + 1] = bf_hi(w[j]);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    const float sbf = __fdiv_rn(amax, six_ts);
+    const uint32_t sbc = pack_e4m3x4(sbf, 0.f, 0.f, 0.f) & 0xffu;
+    scales[b] = (uint8_t)sbc;
+    const float den = __fmul_rn(e4m3_byte_value(sbc), ts);
+    uint2 o;
+    if (den == 0.f) {
+      // signed zeros
+      uint32_t c[2] = {0u, 0u};
+#pragma unroll
+      for (int i = 0; i < 16; ++i) c[i / 8] |= (__float_as_uint(f[i]) >> 31) << (4 * (i % 8) + 3);
+      o = make_uint2(c[0], c[1]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) f[i] = __fdiv_rn(f[i], den);
+      o.x = pack_e2m1x8(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]);
+      o.y = pack_e2m1x8(f[8], f[9], f[10], f[11], f[12], f[13], f[14], f[15]);
+    }
+    reinterpret_cast<uint2*>(codes)[b] = o;
+  }
+}
+
 int grid_for(long long work, int per_cta) {
   int sms = 152;
   int dev = 0;
@@ -227,6 +305,18 @@ cudaError_t launch_quantize_qkv(const void* q, const void* k, const void* v, lon
   if (total > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (d == 128) quant_qkv_kernel<128><<<(unsigned)total, 256, 0, st>>>(p);
   else quant_qkv_kernel<64><<<(unsigned)total, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_nvfp4(const void* x, long long n, void* codes, void* scales, float* ts,
+                                  cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(ts, 0, sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  nvfp4_amax_kernel<<<grid_for(n / 8, 256), 256, 0, st>>>((const uint4*)x, n / 8, reinterpret_cast<unsigned*>(ts));
+  nvfp4_tensor_scale_kernel<<<1, 1, 0, st>>>(ts);
+  const long long nblocks = n / 16;
+  quant_nvfp4_kernel<<<grid_for(nblocks, 256), 256, 0, st>>>((const uint4*)x, nblocks, ts, (uint8_t*)codes,
+                                                            (uint8_t*)scales);
   return cudaGetLastError();
 }
 

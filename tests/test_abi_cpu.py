@@ -61,6 +61,15 @@ def test_argument_errors_before_launch(lib):
     assert lib.fa4fp4_fwd(*args, 1, 4, 4, 64, 64, 0.0, 0, p, 7, null, null) == INVALID # dtype
     assert lib.fa4fp4_fwd(*([p] * 5 + [odd]), 1, 4, 4, 64, 64, 0.0, 0, p, 1, null, null) == ALIGN
     assert lib.fa4bf16_fwd(null, p, p, 1, 1, 1, 64, 64, 0.0, 0, p, 1, null, null) == INVALID
+    assert lib.fa4fp4_quantize_nvfp4(null, 1, 1, 32, 64, p, p, p, null) == INVALID
+    assert lib.fa4fp4_quantize_nvfp4(p, 1, 1, 32, 64, p, p, null, null) == INVALID
+    assert lib.fa4fp4_quantize_nvfp4(p, 1, 1, 32, 96, p, p, p, null) == UNSUP
+    assert lib.fa4fp4_quantize_nvfp4(p, 1, 1, 32, 64, p, p, ctypes.c_void_p(4098), null) == ALIGN
+    nv = [p] * 8
+    assert lib.fa4fp4_fwd_nvfp4(p, p, null, p, p, p, p, p, 1, 4, 2, 64, 64, 0.0, 0, 0, p, 1, null, null) == INVALID
+    assert lib.fa4fp4_fwd_nvfp4(*nv, 1, 4, 2, 64, 64, 0.0, 0, 2, p, 1, null, null) == INVALID   # fp8pv
+    assert lib.fa4fp4_fwd_nvfp4(*nv, 1, 4, 3, 64, 64, 0.0, 0, 0, p, 1, null, null) == UNSUP
+    assert lib.fa4fp4_fwd_fp8pv(*([p] * 6), 1, 4, 4, 64, 80, 0.0, 0, p, 1, null, null) == UNSUP
     qkv = [p] * 3
     outs = [p] * 6
     assert lib.fa4fp4_quantize_qkv(null, p, p, 1, 4, 2, 64, 64, *outs, null) == INVALID

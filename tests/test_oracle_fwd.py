@@ -245,3 +245,25 @@ def test_fp8pv_close_to_softmax():
     e0 = np.linalg.norm(O0 - O1) / np.linalg.norm(O1)
     assert e2 < 0.08 and e2 < e0 / 2
     assert np.max(np.abs(L2 - L1)) < 0.05     # a stray factor (Direct-P's 6) would be ln 6
+
+
+def test_nvfp4_qk_scores_beat_mxfp4_on_outlier_channels():
+    """On the outlier-channel workload's distribution (4 of 128 channels x8 in
+    Q and K), NVFP4 Q/K (a scale per 16 plus a tensor scale) give scores
+    closer to the bf16 scores than MXFP4 (a power-of-two scale per 32)."""
+    from precision_attention_fa4fp4_gb300.inputs import VIDEO_DIT, Workload, make_inputs
+    w = Workload("outliers_small", 1, 2, 2, 512, 128, n_outliers=VIDEO_DIT.n_outliers)
+    q, k, _ = (t.float().numpy() for t in make_inputs(w))
+    S = np.einsum("bhid,bhjd->bhij", q.astype(np.float64), k.astype(np.float64))
+
+    def scores(qd, kd):
+        return np.einsum("bhid,bhjd->bhij", qd.astype(np.float64), kd.astype(np.float64))
+
+    mx = scores(oracle.dequantize(*oracle.quantize(q, 0, 0), q.shape, 0, 0),
+                oracle.dequantize(*oracle.quantize(k, 0, 0), k.shape, 0, 0))
+    cq, sq, tq = oracle.quantize_nvfp4(q)
+    ck, sk, tk = oracle.quantize_nvfp4(k)
+    nv = scores(oracle.dequantize_nvfp4(cq, sq, tq, q.shape), oracle.dequantize_nvfp4(ck, sk, tk, k.shape))
+    e_mx = np.linalg.norm(mx - S) / np.linalg.norm(S)
+    e_nv = np.linalg.norm(nv - S) / np.linalg.norm(S)
+    assert e_nv < e_mx, (e_nv, e_mx)
