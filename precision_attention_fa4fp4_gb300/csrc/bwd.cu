@@ -38,7 +38,7 @@ namespace {
 
 constexpr int BK = 128;          // keys per CTA
 constexpr int BQ = 64;           // queries per step
-constexpr int NST = 4;           // input stages (Q4, dOr, Q8, dOc of a step)
+constexpr int NST = 3;           // input stages (Q4, dOr, Q8, dOc of a step)
 constexpr int D = 128;
 constexpr int NTHREADS = 14 * 32;
 constexpr uint32_t TMEM_COLS = 512;
@@ -61,7 +61,9 @@ struct BL {   // shared-memory layout (bytes)
   // chunk ids: 0 K4, 1 V8, 2 K8, 3-4 P, 5-6 dSc, 7-8 dSr (by step parity),
   // 9 + 4 * stage + {0 Q4, 1 dOr, 2 Q8, 3 dOc}
   static constexpr int VEC = SFC + (9 + 4 * NST) * 512;   // float lse2[NST][64], dvec[NST][64]
-  static constexpr int BAR = VEC + 2 * NST * BQ * 4;
+  static constexpr int DQS = VEC + 2 * NST * BQ * 4;      // dQ tile [64 q][128 d] fp32
+  static constexpr int OKS = DQS + BQ * D * 4;             // int [4]: dQ writers' status
+  static constexpr int BAR = OKS + 16;
   static constexpr int NBAR = 1 + NST + NST + 1 + 1 + 2 + 1 + 1 + 1 + 1;
   static constexpr int MISC = BAR + 8 * NBAR;
   static constexpr int BYTES = MISC + 64 + 1024;
@@ -426,53 +428,51 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
     }
   } else {
     // ------------------------------------------------------------ dQ writer
+    // dQ^T from TMEM, times softmax_scale, staged as a [64 q][128 d] fp32 tile
+    // in shared memory and added into dq by one bulk tensor reduction per step.
     const int quad = warp & 3;
+    const int drow = quad * 32 + lane;
     const uint32_t lane_base = tbase + ((uint32_t)(quad * 32) << 16);
+    float* stage = reinterpret_cast<float*>(smem + BL::DQS);
+    int* okw = reinterpret_cast<int*>(smem + BL::OKS);
+    const bool issuer = warp == 10 && lane == 0;
     for (int t = 0; t < nsteps; ++t) {
       const int h = hk * group + t / per_head;
       const int q0 = (i0 + t % per_head) * BQ;
-      if (!mbar_wait(dq_full, t & 1, abort_flag, p.err)) break;
-      tc_fence_after();
+      // the four writer warps leave together: each publishes its status
+      // before the barrier and all read the four after it
+      const bool wok = mbar_wait(dq_full, t & 1, abort_flag, p.err);
       uint32_t v0[32], v1[32];
-      tmem_ld32(lane_base + COL_DQT, v0);
-      tmem_ld32(lane_base + COL_DQT + 32, v1);
-      tmem_ld_wait();
-      reg_fence32(v0);
-      reg_fence32(v1);
-      tc_fence_before();
+      if (wok) {
+        tc_fence_after();
+        tmem_ld32(lane_base + COL_DQT, v0);
+        tmem_ld32(lane_base + COL_DQT + 32, v1);
+        tmem_ld_wait();
+        reg_fence32(v0);
+        reg_fence32(v1);
+        tc_fence_before();
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(dq_free);
-      // Thread (d row 32*quad + lane) holds dQ[q0 + i][d] for 64 queries i.
-      // 4x4 transposes among the lanes 4a..4a+3 (two butterfly exchanges)
-      // give lane 4a+b the values d = 32*quad + 4a .. +3 of query 4*blk + b,
-      // added into dq with one 16-byte atomic.
-      const int bq = lane & 3, a4 = lane & ~3;
-      float* dst = p.dq + ((long long)(b * p.Hq + h) * p.N + q0) * D + quad * 32 + a4;
-      const int nq = min(BQ, p.N - q0);
+      if (lane == 0 && wok) mbar_arrive(dq_free);
+      // the previous step's reduction has read the staging tile
+      if (issuer) bulk_wait_read0();
+      const bool all_ok = __all_sync(0xffffffffu, wok);
+      if (lane == 0) okw[warp - 10] = all_ok ? 1 : 0;
+      named_bar(1, 128);
+      if (!(okw[0] & okw[1] & okw[2] & okw[3])) break;
 #pragma unroll
-      for (int blk = 0; blk < 16; ++blk) {
-        float e[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int i = 4 * blk + c;
-          e[c] = __uint_as_float(i < 32 ? v0[i] : v1[i - 32]) * p.scale;
-        }
-#pragma unroll
-        for (int k = 1; k <= 2; k <<= 1) {
-          const bool hi = (lane & k) != 0;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if (i & k) continue;
-            const int j = i | k;
-            const float send = hi ? e[i] : e[j];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, k);
-            if (hi) e[i] = recv; else e[j] = recv;
-          }
-        }
-        const int qi = 4 * blk + bq;
-        if (qi < nq) atomicAdd(reinterpret_cast<float4*>(dst + (long long)qi * D), make_float4(e[0], e[1], e[2], e[3]));
+      for (int i = 0; i < 32; ++i) {
+        stage[i * D + drow] = __uint_as_float(v0[i]) * p.scale;
+        stage[(32 + i) * D + drow] = __uint_as_float(v1[i]) * p.scale;
+      }
+      fence_proxy_async_smem();
+      named_bar(1, 128);
+      if (issuer) {
+        tma_reduce_add_3d(&p.tm_dq, stage, 0, q0, b * p.Hq + h);
+        bulk_commit();
       }
     }
+    if (issuer) bulk_wait0();
   }
   tc_fence_before();
   __syncthreads();

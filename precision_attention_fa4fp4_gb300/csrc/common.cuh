@@ -121,6 +121,22 @@ FA4_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c
       : "memory");
 }
 
+// Element-wise add of a shared-memory tile into global memory (bulk tensor
+// reduction; out-of-range rows of the box are not written).  Completion is
+// tracked by the issuing thread's bulk async groups.
+FA4_DEV void tma_reduce_add_3d(const CUtensorMap* map, const void* src_smem, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src_smem)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+FA4_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the issuing thread's bulk groups have finished reading shared memory
+FA4_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... and have completed
+FA4_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 FA4_DEV void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

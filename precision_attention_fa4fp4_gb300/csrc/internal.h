@@ -76,6 +76,7 @@ struct BwdParams {
   CUtensorMap tm_q8c, tm_k8c;        // MXFP8 column views [bh][d][Np]
   CUtensorMap tm_v8r;                // MXFP8 row view of V [bh][N][d]
   CUtensorMap tm_do_r, tm_do_c;      // MXFP8 views of dO (workspace)
+  CUtensorMap tm_dq;                 // dq fp32 [bh][N][d], for bulk reductions
   const uint8_t *q4_s, *k4_s, *q8c_s, *k8c_s, *v8r_s, *do_r_s, *do_c_s;
   const float* lse;
   const float* Dvec;                 // rowsum(dO*O), workspace
