@@ -522,23 +522,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
         tc_fence_after();
         const float alpha = (m_new == m) ? 1.f : ex2_approx(fmaf(m, c, -mc));
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          // the row of O_X and l_X in one TMEM round trip
+          uint32_t ov[D / 32][32];
+#pragma unroll
+          for (int g = 0; g < D / 32; ++g) tmem_ld32(lane_base + COL_O0 + 128 * x + 32 * g, ov[g]);
+          uint32_t lv = tmem_ld1(lane_base + COL_L0 + 16 * x);
+          tmem_ld_wait_regs(ov[0], lv);
 #pragma unroll
           for (int g = 0; g < D / 32; ++g) {
-            uint32_t ov[32];
-            tmem_ld32(lane_base + COL_O0 + 128 * x + 32 * g, ov);
-            tmem_ld_wait();
-            reg_fence32(ov);
+            reg_fence32(ov[g]);
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
-              float2 t = fmul2(make_float2(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1])),
+              float2 t = fmul2(make_float2(__uint_as_float(ov[g][i]), __uint_as_float(ov[g][i + 1])),
                                make_float2(alpha, alpha));
-              ov[i] = __float_as_uint(t.x);
-              ov[i + 1] = __float_as_uint(t.y);
+              ov[g][i] = __float_as_uint(t.x);
+              ov[g][i + 1] = __float_as_uint(t.y);
             }
-            tmem_st32(lane_base + COL_O0 + 128 * x + 32 * g, ov);
+            tmem_st32(lane_base + COL_O0 + 128 * x + 32 * g, ov[g]);
           }
-          const uint32_t lv = tmem_ld1(lane_base + COL_L0 + 16 * x);
-          tmem_ld_wait();
           tmem_st1(lane_base + COL_L0 + 16 * x, __float_as_uint(__uint_as_float(lv) * alpha));
           tmem_st_wait();
         }
