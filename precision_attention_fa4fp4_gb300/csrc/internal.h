@@ -22,7 +22,7 @@ struct QkvParams {
   uint8_t *qc, *qs, *kc, *ks, *vc, *vs;
   int N, Np;
   long long nbq, nbk;          // 32-element blocks of Q and K
-  long long nq_cta, nk_cta;    // CTAs of 256 row blocks
+  long long nq_cta, nk_cta;    // CTAs of 512 row blocks
   long long nv;                // 128-token V tiles
   long long period;            // every period-th CTA (of the first nv) is a V tile
 };

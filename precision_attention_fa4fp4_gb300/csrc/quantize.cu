@@ -32,13 +32,10 @@ FA4_DEV int block_exp(float amax, float* inv) {
   return X;
 }
 
-// blocks along d: one thread per 32-element block b.
+// blocks along d: one thread per 32-element block b, given its 64 bf16 bytes.
 template <int FMT>
-FA4_DEV void quant_row_block(const uint4* __restrict__ x, long long b, uint8_t* __restrict__ codes,
-                             uint8_t* __restrict__ scales) {
-  uint4 v[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) v[i] = __ldg(x + b * 4 + i);
+FA4_DEV void quant_row_block_v(const uint4 (&v)[4], long long b, uint8_t* __restrict__ codes,
+                               uint8_t* __restrict__ scales) {
   float f[32];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -77,6 +74,15 @@ FA4_DEV void quant_row_block(const uint4* __restrict__ x, long long b, uint8_t* 
     reinterpret_cast<uint4*>(codes)[2 * b] = o0;
     reinterpret_cast<uint4*>(codes)[2 * b + 1] = o1;
   }
+}
+
+template <int FMT>
+FA4_DEV void quant_row_block(const uint4* __restrict__ x, long long b, uint8_t* __restrict__ codes,
+                             uint8_t* __restrict__ scales) {
+  uint4 v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __ldg(x + b * 4 + i);
+  quant_row_block_v<FMT>(v, b, codes, scales);
 }
 
 template <int FMT>
@@ -157,7 +163,7 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(const __nv_bfloat16* __
 
 // Q and K (blocks along d) and V (blocks along N) in one grid.  CTA i is a V
 // tile when i is a multiple of `period` (the first nv of them), else a CTA of
-// 256 row blocks of Q, then of K: the transposes of V are spread among the row
+// 512 row blocks of Q, then of K: the transposes of V are spread among the row
 // streams instead of running after them.
 template <int D>
 __global__ void __launch_bounds__(256) quant_qkv_kernel(const QkvParams p) {
@@ -172,13 +178,22 @@ __global__ void __launch_bounds__(256) quant_qkv_kernel(const QkvParams p) {
   }
   const long long before = (i + P - 1) / P;
   const long long r = i - (before < p.nv ? before : p.nv);   // index among the row CTAs
-  if (r < p.nq_cta) {
-    const long long b = r * 256 + threadIdx.x;
-    if (b < p.nbq) quant_row_block<0>(p.q, b, p.qc, p.qs);
-  } else {
-    const long long b = (r - p.nq_cta) * 256 + threadIdx.x;
-    if (b < p.nbk) quant_row_block<0>(p.k, b, p.kc, p.ks);
+  // a row CTA takes 512 blocks: each thread loads two blocks before converting
+  // either, for more bytes in flight
+  const bool isq = r < p.nq_cta;
+  const uint4* x = isq ? p.q : p.k;
+  const long long nb = isq ? p.nbq : p.nbk;
+  const long long b0 = (isq ? r : r - p.nq_cta) * 512 + threadIdx.x, b1 = b0 + 256;
+  uint4 va[4], vb[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    va[t] = b0 < nb ? __ldg(x + b0 * 4 + t) : make_uint4(0, 0, 0, 0);
+    vb[t] = b1 < nb ? __ldg(x + b1 * 4 + t) : make_uint4(0, 0, 0, 0);
   }
+  uint8_t* codes = isq ? p.qc : p.kc;
+  uint8_t* scales = isq ? p.qs : p.ks;
+  if (b0 < nb) quant_row_block_v<0>(va, b0, codes, scales);
+  if (b1 < nb) quant_row_block_v<0>(vb, b1, codes, scales);
 }
 
 // ---------------------------------------------------------------- NVFP4
@@ -297,8 +312,8 @@ cudaError_t launch_quantize_qkv(const void* q, const void* k, const void* v, lon
   p.Np = padded_n(N);
   p.nbq = BHq * N * (d / 32);
   p.nbk = BHkv * N * (d / 32);
-  p.nq_cta = (p.nbq + 255) / 256;
-  p.nk_cta = (p.nbk + 255) / 256;
+  p.nq_cta = (p.nbq + 511) / 512;
+  p.nk_cta = (p.nbk + 511) / 512;
   p.nv = (long long)(p.Np / 128) * BHkv;
   const long long total = p.nv + p.nq_cta + p.nk_cta;
   p.period = total / p.nv;
