@@ -21,9 +21,12 @@
  *     fa4fp4_sync_status.
  *   - Tensors are dense and row-major in the layouts stated below; every
  *     pointer must be 16-byte aligned (FA4FP4_ERR_ALIGNMENT otherwise).
- *   - Supported shapes: d in {64, 128}; N >= 1; B, H >= 0 (0 is a no-op);
- *     Hq % Hkv == 0; causal attention uses the same N for queries and keys,
- *     aligned top-left (key n is visible to query i iff n <= i).
+ *   - Supported shapes: d in {64, 128}; N >= 1; B, H >= 0; Hq % Hkv == 0;
+ *     causal attention uses the same N for queries and keys, aligned top-left
+ *     (key n is visible to query i iff n <= i).
+ *   - An empty problem (B == 0, or H == 0 / Hq == 0) is a no-op: the call
+ *     checks its shape and options, then returns FA4FP4_OK without inspecting
+ *     its pointers (they may be NULL) and without launching anything.
  *   - softmax_scale <= 0 selects 1/sqrt(d).
  *   - No C++ exception crosses this boundary; there is no CPU fallback.
  *

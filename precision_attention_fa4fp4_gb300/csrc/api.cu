@@ -131,12 +131,12 @@ size_t fa4fp4_qtensor_bytes(int B, int H, int N, int d, int fmt, int axis, size_
 
 fa4fp4_status fa4fp4_quantize(const void* x, int B, int H, int N, int d, int fmt, int axis,
                               void* codes, void* scales, void* stream) {
-  if (!x || !codes || !scales) return FA4FP4_ERR_INVALID_ARG;
   if ((fmt != 0 && fmt != 1) || (axis != 0 && axis != 1)) return FA4FP4_ERR_INVALID_ARG;
   fa4fp4_status s = check_dims(B, H, H, N, d);
-  if (s != FA4FP4_OK && !(H == 0 && s == FA4FP4_ERR_UNSUPPORTED)) return s;
-  if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return FA4FP4_ERR_ALIGNMENT;
+  if (s != FA4FP4_OK) return s;
   if (B == 0 || H == 0) return FA4FP4_OK;
+  if (!x || !codes || !scales) return FA4FP4_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return FA4FP4_ERR_ALIGNMENT;
   long long BH = (long long)B * H;
   return launch_status(launch_quantize(x, BH * N, d, N, BH, fmt, axis, codes, scales,
                                        static_cast<cudaStream_t>(stream)));
@@ -145,14 +145,14 @@ fa4fp4_status fa4fp4_quantize(const void* x, int B, int H, int N, int d, int fmt
 fa4fp4_status fa4fp4_quantize_qkv(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,
                                   int N, int d, void* q_codes, void* q_scales, void* k_codes, void* k_scales,
                                   void* vt_codes, void* vt_scales, void* stream) {
-  if (!q || !k || !v || !q_codes || !q_scales || !k_codes || !k_scales || !vt_codes || !vt_scales)
-    return FA4FP4_ERR_INVALID_ARG;
   fa4fp4_status s = check_dims(B, Hq, Hkv, N, d);
   if (s != FA4FP4_OK) return s;
+  if (B == 0 || Hq == 0) return FA4FP4_OK;
   const void* ptrs[] = {q, k, v, q_codes, q_scales, k_codes, k_scales, vt_codes, vt_scales};
   for (const void* ptr : ptrs)
+    if (!ptr) return FA4FP4_ERR_INVALID_ARG;
+  for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return FA4FP4_ERR_ALIGNMENT;
-  if (B == 0 || Hq == 0) return FA4FP4_OK;
   return launch_status(launch_quantize_qkv(q, k, v, (long long)B * Hq, (long long)B * Hkv, N, d, q_codes,
                                            q_scales, k_codes, k_scales, vt_codes, vt_scales,
                                            static_cast<cudaStream_t>(stream)));
@@ -164,18 +164,18 @@ static fa4fp4_status fwd_common(const void* qc, const void* qs, const void* kc, 
                                 const void* vc, const void* vs, int B, int Hq, int Hkv, int N, int d,
                                 float softmax_scale, int causal, void* o, int out_dtype, float* lse,
                                 int fp8pv, const float* ts_q, const float* ts_k, void* stream) {
+  if (out_dtype != FA4FP4_OUT_F32 && out_dtype != FA4FP4_OUT_BF16) return FA4FP4_ERR_INVALID_ARG;
+  fa4fp4_status s = check_dims(B, Hq, Hkv, N, d);
+  if (s != FA4FP4_OK) return s;
+  if (B == 0 || Hq == 0) return FA4FP4_OK;
   if (!qc || !qs || !kc || !ks || !vc || !vs || !o) return FA4FP4_ERR_INVALID_ARG;
   if ((ts_q == nullptr) != (ts_k == nullptr)) return FA4FP4_ERR_INVALID_ARG;
   if ((ts_q && (reinterpret_cast<uintptr_t>(ts_q) & 3)) || (ts_k && (reinterpret_cast<uintptr_t>(ts_k) & 3)))
     return FA4FP4_ERR_ALIGNMENT;
-  if (out_dtype != FA4FP4_OUT_F32 && out_dtype != FA4FP4_OUT_BF16) return FA4FP4_ERR_INVALID_ARG;
-  fa4fp4_status s = check_dims(B, Hq, Hkv, N, d);
-  if (s != FA4FP4_OK) return s;
   const void* ptrs[] = {qc, qs, kc, ks, vc, vs, o};
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return FA4FP4_ERR_ALIGNMENT;
   if (lse && !aligned16(lse)) return FA4FP4_ERR_ALIGNMENT;
-  if (B == 0 || Hq == 0) return FA4FP4_OK;
   FwdFp4Params p;
   memset(&p, 0, sizeof(p));
   const int Np = padded_n(N);
@@ -228,19 +228,21 @@ fa4fp4_status fa4fp4_fwd_nvfp4(const void* qc, const void* qs, const float* q_ts
                                const void* ks, const float* k_ts, const void* vc, const void* vs, int B,
                                int Hq, int Hkv, int N, int d, float softmax_scale, int causal, int fp8pv,
                                void* o, int out_dtype, float* lse, void* stream) {
-  if (!q_ts || !k_ts || (fp8pv != 0 && fp8pv != 1)) return FA4FP4_ERR_INVALID_ARG;
+  if (fp8pv != 0 && fp8pv != 1) return FA4FP4_ERR_INVALID_ARG;
+  const bool empty = B == 0 || Hq == 0;
+  if (!empty && (!q_ts || !k_ts)) return FA4FP4_ERR_INVALID_ARG;
   return fwd_common(qc, qs, kc, ks, vc, vs, B, Hq, Hkv, N, d, softmax_scale, causal, o, out_dtype, lse,
                     fp8pv, q_ts, k_ts, stream);
 }
 
 fa4fp4_status fa4fp4_quantize_nvfp4(const void* x, int B, int H, int N, int d, void* codes, void* scales,
                                     float* ts, void* stream) {
-  if (!x || !codes || !scales || !ts) return FA4FP4_ERR_INVALID_ARG;
   fa4fp4_status s = check_dims(B, H, H, N, d);
-  if (s != FA4FP4_OK && !(H == 0 && s == FA4FP4_ERR_UNSUPPORTED)) return s;
+  if (s != FA4FP4_OK) return s;
+  if (B == 0 || H == 0) return FA4FP4_OK;
+  if (!x || !codes || !scales || !ts) return FA4FP4_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || (reinterpret_cast<uintptr_t>(ts) & 3))
     return FA4FP4_ERR_ALIGNMENT;
-  if (B == 0 || H == 0) return FA4FP4_OK;
   return launch_status(launch_quantize_nvfp4(x, (long long)B * H * N * d, codes, scales, ts,
                                              static_cast<cudaStream_t>(stream)));
 }
@@ -269,16 +271,16 @@ fa4fp4_status fa4fp4_bwd(const void* q4c, const void* q4s, const void* k4c, cons
                          const void* dout, const float* lse, int B, int Hq, int Hkv, int N, int d,
                          float softmax_scale, int causal, float* dq, float* dk, float* dv,
                          void* workspace, size_t workspace_bytes, void* stream) {
-  const void* ptrs[] = {q4c, q4s, k4c, k4s, q8c, q8s, k8c, k8s, v8c, v8s, o, dout, lse, dq, dk, dv};
-  for (const void* ptr : ptrs)
-    if (!ptr) return FA4FP4_ERR_INVALID_ARG;
   if (o_dtype != FA4FP4_OUT_F32 && o_dtype != FA4FP4_OUT_BF16) return FA4FP4_ERR_INVALID_ARG;
   fa4fp4_status s = check_dims(B, Hq, Hkv, N, d);
   if (s != FA4FP4_OK) return s;
   if (d != 128) return FA4FP4_ERR_UNSUPPORTED;
+  if (B == 0 || Hq == 0) return FA4FP4_OK;
+  const void* ptrs[] = {q4c, q4s, k4c, k4s, q8c, q8s, k8c, k8s, v8c, v8s, o, dout, lse, dq, dk, dv};
+  for (const void* ptr : ptrs)
+    if (!ptr) return FA4FP4_ERR_INVALID_ARG;
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return FA4FP4_ERR_ALIGNMENT;
-  if (B == 0 || Hq == 0) return FA4FP4_OK;
   const size_t need = fa4fp4_bwd_workspace_bytes(B, Hq, Hkv, N, d);
   if (!workspace || workspace_bytes < need) return FA4FP4_ERR_WORKSPACE;
   if (!aligned16(workspace)) return FA4FP4_ERR_ALIGNMENT;
@@ -336,13 +338,13 @@ fa4fp4_status fa4fp4_bwd(const void* q4c, const void* q4s, const void* k4c, cons
 fa4fp4_status fa4bf16_fwd(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,
                           int N, int d, float softmax_scale, int causal, void* o, int out_dtype,
                           float* lse, void* stream) {
-  if (!q || !k || !v || !o) return FA4FP4_ERR_INVALID_ARG;
   if (out_dtype != FA4FP4_OUT_F32 && out_dtype != FA4FP4_OUT_BF16) return FA4FP4_ERR_INVALID_ARG;
   fa4fp4_status s = check_dims(B, Hq, Hkv, N, d);
   if (s != FA4FP4_OK) return s;
+  if (B == 0 || Hq == 0) return FA4FP4_OK;
+  if (!q || !k || !v || !o) return FA4FP4_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
     return FA4FP4_ERR_ALIGNMENT;
-  if (B == 0 || Hq == 0) return FA4FP4_OK;
   FwdBf16Params p;
   memset(&p, 0, sizeof(p));
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;

@@ -88,3 +88,39 @@ def test_workspace_size(lib):
     rows = 2 * 4 * 300
     assert n >= rows * 128 + rows * 4 + 2 * 4 * 128 * 384 + rows * 4
     assert lib.fa4fp4_bwd_workspace_bytes(2, 4, 3, 300, 128) == 0
+
+
+def test_empty_problems_are_noops(lib):
+    """B == 0 or H == 0: shape and options are still checked, then the call
+    returns OK without inspecting its (here NULL) pointers or launching."""
+    null = None
+    OK, INVALID, UNSUP = 0, 1, 2
+    n6 = [null] * 6
+    for B, H in ((0, 4), (2, 0)):
+        Hkv = 2 if H else 0
+        assert lib.fa4fp4_quantize(null, B, H, 32, 64, 0, 0, null, null, null) == OK
+        assert lib.fa4fp4_quantize(null, B, H, 32, 128, 1, 1, null, null, null) == OK
+        assert lib.fa4fp4_quantize_qkv(null, null, null, B, H, Hkv, 64, 128, *n6, null) == OK
+        assert lib.fa4fp4_quantize_nvfp4(null, B, H, 32, 64, null, null, null, null) == OK
+        assert lib.fa4fp4_fwd(*n6, B, H, Hkv, 300, 128, 0.0, 1, null, 1, null, null) == OK
+        assert lib.fa4fp4_fwd_fp8pv(*n6, B, H, Hkv, 300, 64, 0.0, 0, null, 0, null, null) == OK
+        assert lib.fa4fp4_fwd_nvfp4(*([null] * 8), B, H, Hkv, 300, 128, 0.0, 1, 1, null, 1, null, null) == OK
+        assert lib.fa4bf16_fwd(null, null, null, B, H, Hkv, 300, 128, 0.0, 1, null, 1, null, null) == OK
+        assert lib.fa4fp4_bwd(*([null] * 11), 0, null, null, B, H, Hkv, 300, 128, 0.0, 1,
+                              null, null, null, null, 0, null) == OK
+        assert lib.fa4fp4_bwd_workspace_bytes(B, H, Hkv, 300, 128) == 0
+    bwd_na = lib.fa4fp4_bwd_noalloc
+    bwd_na.restype = ctypes.c_int
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    bwd_na.argtypes = [vp] * 11 + [i, vp, vp, i, i, i, i, i, f, i, vp, vp, vp, vp]
+    assert bwd_na(*([null] * 11), 0, null, null, 0, 4, 2, 300, 128, 0.0, 1, null, null, null, null) == OK
+    # an empty problem with a bad shape or option is still rejected
+    assert lib.fa4fp4_quantize(null, 0, 4, 32, 96, 0, 0, null, null, null) == UNSUP
+    assert lib.fa4fp4_quantize(null, 0, 4, 0, 64, 0, 0, null, null, null) == INVALID
+    assert lib.fa4fp4_quantize(null, 0, 4, 32, 64, 3, 0, null, null, null) == INVALID
+    assert lib.fa4fp4_fwd(*n6, 0, 4, 3, 64, 64, 0.0, 0, null, 1, null, null) == UNSUP
+    assert lib.fa4fp4_fwd(*n6, 0, 4, 4, 64, 64, 0.0, 0, null, 9, null, null) == INVALID
+    assert lib.fa4fp4_fwd_nvfp4(*([null] * 8), 0, 4, 4, 64, 64, 0.0, 0, 5, null, 1, null, null) == INVALID
+    assert lib.fa4fp4_bwd(*([null] * 11), 0, null, null, 0, 4, 2, 300, 64, 0.0, 1,
+                          null, null, null, null, 0, null) == UNSUP
+    assert lib.fa4fp4_quantize_qkv(null, null, null, -1, 4, 2, 64, 128, *n6, null) == INVALID
