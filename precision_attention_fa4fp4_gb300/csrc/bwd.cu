@@ -380,20 +380,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
       st_row_sw64(dsc, r, g, lo, hi);
       sfc[(3 + sp) * 512 + lane * 16 + quad * 4 + g] = (uint8_t)(xp + 127);
       sfc[(5 + sp) * 512 + lane * 16 + quad * 4 + g] = (uint8_t)(xc + 127);
-      // dS in blocks of 32 keys (the 32 lanes of this warp) per query column
+      // dS in blocks of 32 keys (the 32 lanes of this warp) per query column.
+      // The block exponent rule of e4m3_block_exp, from the biased exponent E
+      // of the column's amax (sign bit clear): X = max(E - 135, -127), so the
+      // factor 2^-X has exponent field min(262 - E, 254) and the scale byte is
+      // X + 127 = max(E, 8) - 8.
       float q8[32];
-      uint32_t my_scale = 0;
+      uint32_t my_e = 0;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const uint32_t am = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(dp[i])));
-        float iv;
-        const int x = e4m3_block_exp(__uint_as_float(am), &iv);
-        q8[i] = dp[i] * iv;
-        if (lane == i) my_scale = (uint32_t)(x + 127);
+        const uint32_t E = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(dp[i]))) >> 23;
+        q8[i] = dp[i] * __uint_as_float(min(262u - E, 254u) << 23);
+        my_e = lane == i ? E : my_e;
       }
       e4m3x32(q8, 1.f, lo, hi);
       st_row_sw64(dsr, r, g, lo, hi);
-      sfc[(7 + sp) * 512 + lane * 16 + g * 4 + quad] = (uint8_t)my_scale;
+      sfc[(7 + sp) * 512 + lane * 16 + g * 4 + quad] = (uint8_t)(max(my_e, 8u) - 8u);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[sp]);
