@@ -39,6 +39,7 @@ namespace {
 constexpr int BK = 128;          // keys per CTA
 constexpr int BQ = 64;           // queries per step
 constexpr int NST = 3;           // input stages (Q4, dOr, Q8, dOc of a step)
+constexpr int BWD_GROUP = 4;     // causal CTA order: kv heads per group
 constexpr int D = 128;
 constexpr int NTHREADS = 14 * 32;
 constexpr uint32_t TMEM_COLS = 512;
@@ -133,8 +134,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
   float* dvec = lse2 + NST * BQ;                               // [NST][64]
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int kt = blockIdx.x;
-  const int bkv = blockIdx.y;
+  // CTA order: groups of G (batch, kv head) pairs, key tile major inside a
+  // group.  Causal (G = BWD_GROUP): key tile 0 has the most query steps, so
+  // the block scheduler starts the longest CTAs of a group first, while only
+  // a few heads' dq rows are being accumulated in L2 at a time.  G = 1 (all
+  // key tiles of one head, then the next) when every CTA has the same work.
+  const int nkt = (p.N + BK - 1) / BK;
+  const int nbkv = p.B * p.Hkv;
+  const int G = p.causal ? min(BWD_GROUP, nbkv) : 1;
+  const int lin = (int)blockIdx.x;
+  const int gbase = (lin / (G * nkt)) * G;
+  const int gsz = min(G, nbkv - gbase);
+  const int rem = lin - gbase * nkt;
+  const int kt = rem / gsz;
+  const int bkv = gbase + rem % gsz;
   const int b = bkv / p.Hkv, hk = bkv % p.Hkv;
   const int group = p.Hq / p.Hkv;
   const int k0 = kt * BK;
@@ -528,7 +541,7 @@ cudaError_t launch_bwd_prep(const BwdPrepParams& p, cudaStream_t st) {
 }
 
 cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t st) {
-  dim3 grid((p.N + BK - 1) / BK, p.B * p.Hkv);
+  const dim3 grid((unsigned)((p.N + BK - 1) / BK) * (unsigned)(p.B * p.Hkv));
   cudaFuncSetAttribute(bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BL::BYTES);
   bwd_kernel<<<grid, NTHREADS, BL::BYTES, st>>>(p);
   return cudaGetLastError();

@@ -69,8 +69,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_bf16_kernel(const __grid_cons
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nq = (p.N + BM - 1) / BM;
-  const int qt = p.causal ? (nq - 1 - (int)blockIdx.x) : (int)blockIdx.x;
-  const int bh = blockIdx.y;
+  // causal: x runs over (batch, head), y over query tiles, longest first
+  const int qt = p.causal ? (nq - 1 - (int)blockIdx.y) : (int)blockIdx.x;
+  const int bh = p.causal ? (int)blockIdx.x : (int)blockIdx.y;
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int bkv = b * p.Hkv + h / (p.Hq / p.Hkv);
   const int q0 = qt * BM;
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_bf16_kernel(const __grid_cons
 
 cudaError_t launch_fwd_bf16(const FwdBf16Params& p, cudaStream_t st) {
   const int nq = (p.N + BM - 1) / BM;
-  dim3 grid(nq, p.B * p.Hq);
+  const dim3 grid = p.causal ? dim3(p.B * p.Hq, nq) : dim3(nq, p.B * p.Hq);
   if (p.d == 128) {
     auto k = fwd_bf16_kernel<128>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemB<128>::BYTES);

@@ -187,8 +187,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nq = (p.N + BM - 1) / BM;
   const int npair = (nq + 1) / 2;
-  const int pair = p.causal ? (npair - 1 - (int)blockIdx.x) : (int)blockIdx.x;
-  const int bh = blockIdx.y;
+  // causal: the grid's x runs over (batch, head) and its y over query-tile
+  // pairs, the pair with the most key tiles first, so that the block scheduler
+  // starts the longest CTAs of every head before any shorter one
+  const int pair = p.causal ? (npair - 1 - (int)blockIdx.y) : (int)blockIdx.x;
+  const int bh = p.causal ? (int)blockIdx.x : (int)blockIdx.y;
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int bkv = b * p.Hkv + h / (p.Hq / p.Hkv);
   const int q0 = pair * 2 * BM;              // first row of tile A; tile B follows
@@ -641,7 +644,7 @@ template <int D, bool P8, bool NV>
 static cudaError_t launch_fwd_t(const FwdFp4Params& p, cudaStream_t st) {
   using L = Layout<D, P8, NV>;
   const int nq = (p.N + BM - 1) / BM;
-  dim3 grid((nq + 1) / 2, p.B * p.Hq);
+  const dim3 grid = p.causal ? dim3(p.B * p.Hq, (nq + 1) / 2) : dim3((nq + 1) / 2, p.B * p.Hq);
   auto k = fwd_fp4_kernel<D, P8, NV>;
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
   k<<<grid, NTHREADS, L::BYTES, st>>>(p);
