@@ -8,7 +8,7 @@
 // Formats"); the abstract adds FP8 gradient operands for P, dS and dO.
 //
 // bwd_prep_kernel: D_i = sum_t dO_it O_it and zeroes dq (the main kernel
-//   accumulates dq with atomics).  The MXFP8 views of dO come from the
+//   adds into dq with bulk tensor reductions).  The MXFP8 views of dO come from the
 //   quantize kernels.
 // bwd_kernel: one CTA per (batch, kv head, 128-key tile); loop over the query
 //   heads of the GQA group x 64-query tiles (causal: from the diagonal on).
