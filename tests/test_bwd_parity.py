@@ -81,3 +81,9 @@ def test_train_causal_gqa_sampled():
     qbase = heads[0] * w.N
     qrows = np.concatenate([qbase + np.arange(0, 128), qbase + np.arange(4096, 4224)])
     check(w, qrows=qrows, krows=krows, heads_for_fwd=heads)
+
+
+def test_causal_gqa_partial_cta_group():
+    """Six (batch, kv head) pairs: the causal backward orders its CTAs in groups
+    of four pairs, so the last group holds two; ragged N (three key tiles)."""
+    check(Workload("bwd_b2_hq6_hkv3_n300", 2, 6, 3, 300, 128, causal=True, qk_std=128 ** -0.25), seed=7)
