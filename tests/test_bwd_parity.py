@@ -6,6 +6,7 @@ dQ, dK, dV (FP32 outputs).
 """
 import numpy as np
 import pytest
+import torch
 
 import oracle
 from gpu_util import assert_close, require_gpu
@@ -14,14 +15,14 @@ from precision_attention_fa4fp4_gb300.inputs import TRAIN_8B, Workload, make_inp
 pytestmark = pytest.mark.gpu
 
 
-def gpu_grads(fa, q, k, v, do, causal):
+def gpu_grads(fa, q, k, v, do, causal, o_bf16=False):
     q, k, v, do = (t.cuda() for t in (q, k, v, do))
     q4, k4 = fa.quantize(q), fa.quantize(k)
     vt = fa.quantize(v, fa.FMT_MXFP4, fa.ALONG_N)
     q8c = fa.quantize(q, fa.FMT_MXFP8, fa.ALONG_N)
     k8c = fa.quantize(k, fa.FMT_MXFP8, fa.ALONG_N)
     v8r = fa.quantize(v, fa.FMT_MXFP8, fa.ALONG_D)
-    o, lse = fa.fwd(q4, k4, vt, causal=causal, out_dtype=fa.OUT_F32)
+    o, lse = fa.fwd(q4, k4, vt, causal=causal, out_dtype=fa.OUT_BF16 if o_bf16 else fa.OUT_F32)
     dq, dk, dv = fa.bwd(q4, k4, q8c, k8c, v8r, o, do, lse, causal=causal)
     fa.sync_status()
     return dq.cpu().numpy(), dk.cpu().numpy(), dv.cpu().numpy()
@@ -38,10 +39,10 @@ def oracle_views(q, k, v):
     return Q4, K4, V4, Q8, K8, V8
 
 
-def check(w: Workload, qrows=None, krows=None, heads_for_fwd=None, seed=0):
+def check(w: Workload, qrows=None, krows=None, heads_for_fwd=None, seed=0, o_bf16=False):
     fa = require_gpu()
     q, k, v, do = make_inputs(w, seed=seed, with_dout=True)
-    dq, dk, dv = gpu_grads(fa, q, k, v, do, w.causal)
+    dq, dk, dv = gpu_grads(fa, q, k, v, do, w.causal, o_bf16)
     Q4, K4, V4, Q8, K8, V8 = oracle_views(q, k, v)
     if heads_for_fwd is None:
         rows = None
@@ -54,6 +55,8 @@ def check(w: Workload, qrows=None, krows=None, heads_for_fwd=None, seed=0):
     Of[idx] = O.astype(np.float32)
     Lf[idx] = L.astype(np.float32)
     Of = Of.reshape(w.B, w.Hq, w.N, w.d)
+    if o_bf16:   # the backward then reads O as the forward wrote it: bf16
+        Of = torch.from_numpy(Of).to(torch.bfloat16).float().numpy()
     Lf = Lf.reshape(w.B, w.Hq, w.N)
     dQ, dK, dV = oracle.bwd(Q4, K4, Q8, K8, V8, Of, do.float().numpy(), Lf, causal=w.causal,
                             qrows=qrows, krows=krows)
@@ -87,3 +90,15 @@ def test_causal_gqa_partial_cta_group():
     """Six (batch, kv head) pairs: the causal backward orders its CTAs in groups
     of four pairs, so the last group holds two; ragged N (three key tiles)."""
     check(Workload("bwd_b2_hq6_hkv3_n300", 2, 6, 3, 300, 128, causal=True, qk_std=128 ** -0.25), seed=7)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_o_in_bf16(causal):
+    """O handed to the backward in bf16 (the preprocess widens it for D)."""
+    check(Workload("bwd_bf16o_n300", 1, 4, 2, 300, 128, causal=causal, qk_std=128 ** -0.25), seed=11,
+          o_bf16=True)
+
+
+def test_mqa_causal():
+    """One kv head shared by eight query heads: dK and dV sum over all eight."""
+    check(Workload("bwd_mqa_n200", 1, 8, 1, 200, 128, causal=True, qk_std=128 ** -0.25), seed=13)

@@ -55,6 +55,14 @@ def test_ragged(N, d, causal):
     check(Workload(f"ragged_n{N}_d{d}", 1, 4, 2, N, d, causal=causal), out_bf16=False, seed=N)
 
 
+@pytest.mark.parametrize("B,Hq,Hkv", [(2, 3, 3), (1, 8, 1), (2, 6, 2)], ids=["mha", "mqa", "gqa3"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_groupings(B, Hq, Hkv, causal):
+    """kv head = h / (Hq / Hkv) for MHA, MQA and groups of three, across batches."""
+    check(Workload(f"heads_b{B}_hq{Hq}_hkv{Hkv}", B, Hq, Hkv, 300, 128, causal=causal), out_bf16=True,
+          seed=B * 100 + Hq * 10 + Hkv)
+
+
 def test_noncausal_4k_sampled():
     check(FWD_4K, True, rows=sample_rows(FWD_4K, tiles_per_head=3, heads=range(0, 64, 9)))
 
