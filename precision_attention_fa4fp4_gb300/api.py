@@ -118,6 +118,42 @@ def qtensor_shapes(B, H, N, d, fmt, axis):
     return (B, H, R, per), (B, H, R, L // 32)
 
 
+def _numel(shape) -> int:
+    n = 1
+    for x in shape:
+        n *= x
+    return n
+
+
+def _expect_qt(name: str, t: QTensor, fmt: int, axis: int, shape: tuple):
+    """The library reads exactly qtensor_shapes(...) bytes of codes and scales:
+    refuse a tensor of another format, axis or size before any launch."""
+    if not isinstance(t, QTensor):
+        raise ValueError(f"{name}: expected a QTensor")
+    kind = ("MXFP4" if fmt == FMT_MXFP4 else "MXFP8") + (" along d" if axis == ALONG_D else " along N")
+    if t.fmt != fmt or t.axis != axis:
+        raise ValueError(f"{name}: expected {kind}")
+    cs, ss = qtensor_shapes(*shape, fmt, axis)
+    if (tuple(t.shape) != tuple(shape) or t.codes.dtype != torch.uint8 or t.scales.dtype != torch.uint8
+            or t.codes.numel() != _numel(cs) or t.scales.numel() != _numel(ss)):
+        raise ValueError(f"{name}: codes/scales are not those of a {kind} tensor of shape {tuple(shape)}")
+
+
+def _expect(name: str, t, shape: tuple, dtypes):
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape) or t.dtype not in dtypes:
+        raise ValueError(f"{name}: expected shape {tuple(shape)} and dtype in {[str(x) for x in dtypes]}, "
+                         f"got {tuple(t.shape)} {t.dtype}")
+
+
+def _expect_out(out, lse, B, Hq, N, d, out_dtype):
+    if out_dtype not in (OUT_F32, OUT_BF16):
+        raise ValueError("out_dtype must be OUT_F32 or OUT_BF16")
+    _expect("out", out, (B, Hq, N, d), (torch.bfloat16,) if out_dtype == OUT_BF16 else (torch.float32,))
+    _expect("lse", lse, (B, Hq, N), (torch.float32,))
+
+
 def qtensor_alloc(B, H, N, d, fmt, axis, device="cuda") -> QTensor:
     cs, ss = qtensor_shapes(B, H, N, d, fmt, axis)
     return QTensor(torch.empty(cs, dtype=torch.uint8, device=device),
@@ -128,8 +164,11 @@ def quantize(x: torch.Tensor, fmt: int = FMT_MXFP4, axis: int = ALONG_D, out: QT
     """Block-quantize a bf16 [B,H,N,d] CUDA tensor (fa4fp4_quantize)."""
     if x.dtype != torch.bfloat16 or x.dim() != 4:
         raise ValueError("quantize expects a bf16 [B,H,N,d] tensor")
-    _cuda(x)
     B, H, N, d = x.shape
+    if out is not None:
+        _expect_qt("out", out, fmt, axis, (B, H, N, d))
+        _cuda(out.codes, out.scales)
+    _cuda(x)
     q = out if out is not None else qtensor_alloc(B, H, N, d, fmt, axis, x.device)
     _check("fa4fp4_quantize", load_library().fa4fp4_quantize(
         _ptr(x), B, H, N, d, fmt, axis, _ptr(q.codes), _ptr(q.scales), _stream(x.device)))
@@ -142,11 +181,16 @@ def quantize_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out=None):
     for t in (q, k, v):
         if t.dtype != torch.bfloat16 or t.dim() != 4:
             raise ValueError("quantize_qkv expects bf16 [B,H,N,d] tensors")
-        _cuda(t)
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
     if k.shape != (B, Hkv, N, d) or v.shape != k.shape:
         raise ValueError("quantize_qkv: k and v must be [B,Hkv,N,d] with q's B, N, d")
+    if out is not None:
+        _expect_qt("out[0] (q)", out[0], FMT_MXFP4, ALONG_D, (B, Hq, N, d))
+        _expect_qt("out[1] (k)", out[1], FMT_MXFP4, ALONG_D, (B, Hkv, N, d))
+        _expect_qt("out[2] (v)", out[2], FMT_MXFP4, ALONG_N, (B, Hkv, N, d))
+        _cuda(*_qt_buffers(*out))
+    _cuda(q, k, v)
     if out is None:
         out = (qtensor_alloc(B, Hq, N, d, FMT_MXFP4, ALONG_D, q.device),
                qtensor_alloc(B, Hkv, N, d, FMT_MXFP4, ALONG_D, q.device),
@@ -163,6 +207,10 @@ def fwd(q: QTensor, k: QTensor, vt: QTensor, causal: bool = False, softmax_scale
     """Direct-P FP4 forward (fa4fp4_fwd).  Returns (o, lse or None)."""
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
+    _expect_qt("q", q, FMT_MXFP4, ALONG_D, (B, Hq, N, d))
+    _expect_qt("k", k, FMT_MXFP4, ALONG_D, (B, Hkv, N, d))
+    _expect_qt("vt", vt, FMT_MXFP4, ALONG_N, (B, Hkv, N, d))
+    _expect_out(out, lse if with_lse else None, B, Hq, N, d, out_dtype)
     dev = q.codes.device
     if out is None:
         out = torch.empty((B, Hq, N, d), dtype=torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32, device=dev)
@@ -180,10 +228,12 @@ def fwd_fp8pv(q: QTensor, k: QTensor, v8t: QTensor, causal: bool = False, softma
               out_dtype: int = OUT_BF16, with_lse: bool = True, out=None, lse=None):
     """FP8 P/V route of the forward (fa4fp4_fwd_fp8pv): MXFP4 Q/K, V as MXFP8
     blocked along N.  Returns (o, lse or None)."""
-    if v8t.fmt != FMT_MXFP8 or v8t.axis != ALONG_N:
-        raise ValueError("fwd_fp8pv expects V quantized to MXFP8 with blocks along N")
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
+    _expect_qt("q", q, FMT_MXFP4, ALONG_D, (B, Hq, N, d))
+    _expect_qt("k", k, FMT_MXFP4, ALONG_D, (B, Hkv, N, d))
+    _expect_qt("v8t", v8t, FMT_MXFP8, ALONG_N, (B, Hkv, N, d))
+    _expect_out(out, lse if with_lse else None, B, Hq, N, d, out_dtype)
     dev = q.codes.device
     if out is None:
         out = torch.empty((B, Hq, N, d), dtype=torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32, device=dev)
@@ -207,12 +257,25 @@ class NvTensor:
     shape: tuple
 
 
+def _expect_nv(name: str, t: NvTensor, shape: tuple):
+    B, H, N, d = shape
+    if not isinstance(t, NvTensor):
+        raise ValueError(f"{name}: expected an NvTensor")
+    if (tuple(t.shape) != tuple(shape) or t.codes.dtype != torch.uint8 or t.scales.dtype != torch.uint8
+            or t.codes.numel() != B * H * N * d // 2 or t.scales.numel() != B * H * N * d // 16
+            or t.ts.dtype != torch.float32 or t.ts.numel() < 1):
+        raise ValueError(f"{name}: codes/scales/ts are not those of an NVFP4 tensor of shape {tuple(shape)}")
+
+
 def quantize_nvfp4(x: torch.Tensor, out: NvTensor | None = None) -> NvTensor:
     """NVFP4 along d of a bf16 [B,H,N,d] CUDA tensor (fa4fp4_quantize_nvfp4)."""
     if x.dtype != torch.bfloat16 or x.dim() != 4:
         raise ValueError("quantize_nvfp4 expects a bf16 [B,H,N,d] tensor")
-    _cuda(x)
     B, H, N, d = x.shape
+    if out is not None:
+        _expect_nv("out", out, (B, H, N, d))
+        _cuda(out.codes, out.scales, out.ts)
+    _cuda(x)
     if out is None:
         out = NvTensor(torch.empty((B, H, N, d // 2), dtype=torch.uint8, device=x.device),
                        torch.empty((B, H, N, d // 16), dtype=torch.uint8, device=x.device),
@@ -226,11 +289,15 @@ def fwd_nvfp4(q: NvTensor, k: NvTensor, vt: QTensor, causal: bool = False, softm
               out_dtype: int = OUT_BF16, with_lse: bool = True, out=None, lse=None):
     """Forward with NVFP4 Q/K (fa4fp4_fwd_nvfp4).  vt MXFP4 along N gives
     Direct-P, MXFP8 along N the FP8 P/V route.  Returns (o, lse or None)."""
-    if vt.axis != ALONG_N:
-        raise ValueError("fwd_nvfp4 expects V blocked along N")
+    if not isinstance(vt, QTensor) or vt.fmt not in (FMT_MXFP4, FMT_MXFP8):
+        raise ValueError("vt: expected an MXFP4 or MXFP8 QTensor blocked along N")
     fp8pv = 1 if vt.fmt == FMT_MXFP8 else 0
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
+    _expect_nv("q", q, (B, Hq, N, d))
+    _expect_nv("k", k, (B, Hkv, N, d))
+    _expect_qt("vt", vt, vt.fmt, ALONG_N, (B, Hkv, N, d))
+    _expect_out(out, lse if with_lse else None, B, Hq, N, d, out_dtype)
     dev = q.codes.device
     if out is None:
         out = torch.empty((B, Hq, N, d), dtype=torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32, device=dev)
@@ -244,6 +311,30 @@ def fwd_nvfp4(q: NvTensor, k: NvTensor, vt: QTensor, causal: bool = False, softm
     return out, (lse if with_lse else None)
 
 
+def _expect_bwd_inputs(q4, k4, q8c, k8c, v8r, o, dout, lse):
+    B, Hq, N, d = q4.shape
+    Hkv = k4.shape[1]
+    _expect_qt("q4", q4, FMT_MXFP4, ALONG_D, (B, Hq, N, d))
+    _expect_qt("k4", k4, FMT_MXFP4, ALONG_D, (B, Hkv, N, d))
+    _expect_qt("q8c", q8c, FMT_MXFP8, ALONG_N, (B, Hq, N, d))
+    _expect_qt("k8c", k8c, FMT_MXFP8, ALONG_N, (B, Hkv, N, d))
+    _expect_qt("v8r", v8r, FMT_MXFP8, ALONG_D, (B, Hkv, N, d))
+    _expect("o", o, (B, Hq, N, d), (torch.float32, torch.bfloat16))
+    _expect("dout", dout, (B, Hq, N, d), (torch.bfloat16,))
+    _expect("lse", lse, (B, Hq, N), (torch.float32,))
+    return B, Hq, Hkv, N, d
+
+
+def _qt_buffers(*qts):
+    return [b for t in qts for b in (t.codes, t.scales)]
+
+
+def _expect_grads(dq, dk, dv, B, Hq, Hkv, N, d):
+    _expect("dq", dq, (B, Hq, N, d), (torch.float32,))
+    _expect("dk", dk, (B, Hkv, N, d), (torch.float32,))
+    _expect("dv", dv, (B, Hkv, N, d), (torch.float32,))
+
+
 def bwd_workspace_bytes(B, Hq, Hkv, N, d) -> int:
     return int(load_library().fa4fp4_bwd_workspace_bytes(B, Hq, Hkv, N, d))
 
@@ -252,8 +343,9 @@ def bwd(q4: QTensor, k4: QTensor, q8c: QTensor, k8c: QTensor, v8r: QTensor, o: t
         dout: torch.Tensor, lse: torch.Tensor, causal: bool = True, softmax_scale: float = 0.0,
         workspace: torch.Tensor | None = None):
     """Quantized backward (fa4fp4_bwd).  Returns (dq, dk, dv) in float32."""
-    B, Hq, N, d = q4.shape
-    Hkv = k4.shape[1]
+    B, Hq, Hkv, N, d = _expect_bwd_inputs(q4, k4, q8c, k8c, v8r, o, dout, lse)
+    if workspace is not None and workspace.dtype != torch.uint8:
+        raise ValueError("workspace: expected a uint8 tensor")
     dev = dout.device
     dq = torch.empty((B, Hq, N, d), dtype=torch.float32, device=dev)
     dk = torch.empty((B, Hkv, N, d), dtype=torch.float32, device=dev)
@@ -262,7 +354,7 @@ def bwd(q4: QTensor, k4: QTensor, q8c: QTensor, k8c: QTensor, v8r: QTensor, o: t
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     o_dtype = OUT_BF16 if o.dtype == torch.bfloat16 else OUT_F32
-    _cuda(o, dout, lse, workspace)
+    _cuda(*_qt_buffers(q4, k4, q8c, k8c, v8r), o, dout, lse, workspace)
     _check("fa4fp4_bwd", load_library().fa4fp4_bwd(
         _ptr(q4.codes), _ptr(q4.scales), _ptr(k4.codes), _ptr(k4.scales), _ptr(q8c.codes), _ptr(q8c.scales),
         _ptr(k8c.codes), _ptr(k8c.scales), _ptr(v8r.codes), _ptr(v8r.scales), _ptr(o), o_dtype, _ptr(dout),
@@ -274,9 +366,15 @@ def bwd(q4: QTensor, k4: QTensor, q8c: QTensor, k8c: QTensor, v8r: QTensor, o: t
 def bf16_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
              softmax_scale: float = 0.0, out_dtype: int = OUT_BF16, with_lse: bool = True, out=None, lse=None):
     """BF16 FlashAttention forward (fa4bf16_fwd).  Returns (o, lse or None)."""
-    _cuda(q, k, v)
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("bf16_fwd expects [B,H,N,d] tensors")
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
+    _expect("q", q, (B, Hq, N, d), (torch.bfloat16,))
+    _expect("k", k, (B, Hkv, N, d), (torch.bfloat16,))
+    _expect("v", v, (B, Hkv, N, d), (torch.bfloat16,))
+    _expect_out(out, lse if with_lse else None, B, Hq, N, d, out_dtype)
+    _cuda(q, k, v)
     if out is None:
         out = torch.empty((B, Hq, N, d), dtype=torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32, device=q.device)
     if with_lse and lse is None:
@@ -329,14 +427,14 @@ def bwd_noalloc(q4: QTensor, k4: QTensor, q8c: QTensor, k8c: QTensor, v8r: QTens
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     fn.restype = i
     fn.argtypes = [vp] * 11 + [i, vp, vp, i, i, i, i, i, f, i, vp, vp, vp, vp]
-    B, Hq, N, d = q4.shape
-    Hkv = k4.shape[1]
+    B, Hq, Hkv, N, d = _expect_bwd_inputs(q4, k4, q8c, k8c, v8r, o, dout, lse)
+    _expect_grads(dq, dk, dv, B, Hq, Hkv, N, d)
     dev = dout.device
     dq = dq if dq is not None else torch.empty((B, Hq, N, d), dtype=torch.float32, device=dev)
     dk = dk if dk is not None else torch.empty((B, Hkv, N, d), dtype=torch.float32, device=dev)
     dv = dv if dv is not None else torch.empty((B, Hkv, N, d), dtype=torch.float32, device=dev)
     o_dtype = OUT_BF16 if o.dtype == torch.bfloat16 else OUT_F32
-    _cuda(o, dout, lse, dq, dk, dv)
+    _cuda(*_qt_buffers(q4, k4, q8c, k8c, v8r), o, dout, lse, dq, dk, dv)
     _check("fa4fp4_bwd_noalloc", fn(
         _ptr(q4.codes), _ptr(q4.scales), _ptr(k4.codes), _ptr(k4.scales), _ptr(q8c.codes), _ptr(q8c.scales),
         _ptr(k8c.codes), _ptr(k8c.scales), _ptr(v8r.codes), _ptr(v8r.scales), _ptr(o), o_dtype, _ptr(dout),
