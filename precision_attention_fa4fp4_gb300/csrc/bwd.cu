@@ -79,8 +79,8 @@ FA4_DEV int e4m3_block_exp(float amax, float* inv) {
 }
 
 // scale words of `nrows` rows, `bpr` bytes each (<= 4), into a chunk
-FA4_DEV void stage_chunk(uint8_t* chunk, const uint8_t* src, long long stride, int nvalid,
-                         int bpr, int lane) {
+// The loads of stage_chunk alone: this lane's 16-byte word of the chunk.
+FA4_DEV uint4 load_chunk(const uint8_t* __restrict__ src, long long stride, int nvalid, int bpr, int lane) {
   uint32_t w[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
@@ -88,11 +88,16 @@ FA4_DEV void stage_chunk(uint8_t* chunk, const uint8_t* src, long long stride, i
     uint32_t v = 0;
     if (r < nvalid) {
       const uint8_t* p = src + r * stride;
-      v = bpr == 4 ? *reinterpret_cast<const uint32_t*>(p) : (uint32_t)*reinterpret_cast<const uint16_t*>(p);
+      v = bpr == 4 ? __ldg(reinterpret_cast<const uint32_t*>(p)) : (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(p));
     }
     w[c] = v;
   }
-  *reinterpret_cast<uint4*>(chunk + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+FA4_DEV void stage_chunk(uint8_t* chunk, const uint8_t* src, long long stride, int nvalid,
+                         int bpr, int lane) {
+  *reinterpret_cast<uint4*>(chunk + lane * 16) = load_chunk(src, stride, nvalid, bpr, lane);
 }
 
 // 32 floats * inv -> 32 E4M3 codes as two uint4 (element 0 in byte 0)
@@ -157,8 +162,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
   const int nsteps = group * per_head;
 
   if (threadIdx.x == 0) {
-    mbar_init(fix_full, 1);
-    for (int s = 0; s < NST; ++s) { mbar_init(&in_full[s], 1); mbar_init(&in_empty[s], 1); }
+    // fix_full, in_full: the producer's two arrivals, one with the tile bytes
+    // before the TMA loads and one after its own shared-memory writes
+    mbar_init(fix_full, 2);
+    for (int s = 0; s < NST; ++s) { mbar_init(&in_full[s], 2); mbar_init(&in_empty[s], 1); }
     mbar_init(s_full, 1);
     mbar_init(st_free, 8);
     mbar_init(&p_full[0], 8);
@@ -178,18 +185,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // The tile loads go first; the scale chunks (plain loads by the warp)
+    // are fetched while they are in flight.
     const int nk_valid = min(BK, p.N - k0);
-    stage_chunk(sfc + 0 * 512, p.k4_s + ((long long)bkv * p.N + k0) * (D / 32), D / 32, nk_valid, 4, lane);
-    stage_chunk(sfc + 1 * 512, p.v8r_s + ((long long)bkv * p.N + k0) * (D / 32), D / 32, nk_valid, 4, lane);
-    stage_chunk(sfc + 2 * 512, p.k8c_s + (long long)bkv * D * (p.Np / 32) + k0 / 32, p.Np / 32, D, 4, lane);
-    fence_proxy_async_smem();
-    __syncwarp();
     if (lane == 0) {
       mbar_arrive_expect_tx(fix_full, BK * D / 2 + BK * D + D * BK);
       tma_load_3d(smem + BL::K4, &p.tm_k4, fix_full, 0, k0, bkv);
       tma_load_3d(smem + BL::V8, &p.tm_v8r, fix_full, 0, k0, bkv);
       tma_load_3d(smem + BL::K8, &p.tm_k8c, fix_full, k0, 0, bkv);
     }
+    stage_chunk(sfc + 0 * 512, p.k4_s + ((long long)bkv * p.N + k0) * (D / 32), D / 32, nk_valid, 4, lane);
+    stage_chunk(sfc + 1 * 512, p.v8r_s + ((long long)bkv * p.N + k0) * (D / 32), D / 32, nk_valid, 4, lane);
+    stage_chunk(sfc + 2 * 512, p.k8c_s + (long long)bkv * D * (p.Np / 32) + k0 / 32, p.Np / 32, D, 4, lane);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(fix_full);
     int issued = 0;
     for (int t = 0; t < nsteps; ++t) {
       const int st = t % NST;
@@ -198,25 +208,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
       const int bh = b * p.Hq + h;
       if (t >= NST && !mbar_wait(&in_empty[st], ((t / NST) - 1) & 1, abort_flag, p.err)) break;
       const int nq_valid = min(BQ, p.N - q0);
-      uint8_t* sc = sfc + (9 + 4 * st) * 512;
-      stage_chunk(sc, p.q4_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, 4, lane);
-      stage_chunk(sc + 512, p.do_r_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, 4, lane);
-      stage_chunk(sc + 1024, p.q8c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
-      stage_chunk(sc + 1536, p.do_c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int qq = lane + 32 * u;
-        const int q = q0 + qq;
-        float l2 = 0.f, dd = 0.f;
-        if (q < p.N) {
-          l2 = p.lse[(long long)bh * p.N + q] * p.l2e;
-          dd = p.Dvec[(long long)bh * p.N + q];
-        }
-        lse2[st * BQ + qq] = l2;
-        dvec[st * BQ + qq] = dd;
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
       if (lane == 0) {
         uint8_t* sb = smem + BL::STG + st * BL::STAGE_BYTES;
         mbar_arrive_expect_tx(&in_full[st], BL::STAGE_BYTES);
@@ -225,6 +216,32 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
         tma_load_3d(sb + BL::Q8, &p.tm_q8c, &in_full[st], q0, 0, bh);
         tma_load_3d(sb + BL::DOC, &p.tm_do_c, &in_full[st], q0, 0, bh);
       }
+      // scale chunks, LSE log2 e and D of the stage, while its tiles are in
+      // flight: every load is issued before the first shared-memory store
+      uint8_t* sc = sfc + (9 + 4 * st) * 512;
+      const uint4 c0 = load_chunk(p.q4_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, 4, lane);
+      const uint4 c1 = load_chunk(p.do_r_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, 4, lane);
+      const uint4 c2 = load_chunk(p.q8c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
+      const uint4 c3 = load_chunk(p.do_c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
+      float l2[2], dd[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int q = q0 + lane + 32 * u;
+        l2[u] = q < p.N ? __ldg(p.lse + (long long)bh * p.N + q) * p.l2e : 0.f;
+        dd[u] = q < p.N ? __ldg(p.Dvec + (long long)bh * p.N + q) : 0.f;
+      }
+      reinterpret_cast<uint4*>(sc)[lane] = c0;
+      reinterpret_cast<uint4*>(sc + 512)[lane] = c1;
+      reinterpret_cast<uint4*>(sc + 1024)[lane] = c2;
+      reinterpret_cast<uint4*>(sc + 1536)[lane] = c3;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        lse2[st * BQ + lane + 32 * u] = l2[u];
+        dvec[st * BQ + lane + 32 * u] = dd[u];
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&in_full[st]);
       issued = t + 1;
     }
     if (*abort_flag && lane == 0) {
