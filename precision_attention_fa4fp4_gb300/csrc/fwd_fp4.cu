@@ -240,14 +240,32 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
     }
+    // Q_A, Q_B scales: 4-byte words by cp.async, completing on q_full with the
+    // tiles, so that the tile loads are not held behind them; the 2-byte
+    // words of d = 64 by plain loads
     const uint8_t* qs = p.q_scales + (long long)bh * p.N * QSB;
+    if constexpr (QSB >= 4) {
 #pragma unroll
-    for (int x = 0; x < 2; ++x)
+      for (int x = 0; x < 2; ++x)
 #pragma unroll
-      for (int k = 0; k < NSC; ++k)
-        stage_sf_rows(smem + L::SF_Q + (x * NSC + k) * 512, qs, q0 + x * BM, min(BM, p.N - q0 - x * BM), QSB,
-                      lane, 4 * k);
-    fence_proxy_async_smem();
+        for (int k = 0; k < NSC; ++k)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int row = q0 + x * BM + lane + 32 * c;
+            const bool in = row < p.N;
+            cp_async4(smem + L::SF_Q + (x * NSC + k) * 512 + lane * 16 + 4 * c,
+                      qs + (long long)(in ? row : 0) * QSB + 4 * k, in ? 4u : 0u);
+          }
+      cp_async_mbar_arrive(q_full);
+    } else {
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+#pragma unroll
+        for (int k = 0; k < NSC; ++k)
+          stage_sf_rows(smem + L::SF_Q + (x * NSC + k) * 512, qs, q0 + x * BM, min(BM, p.N - q0 - x * BM), QSB,
+                        lane, 4 * k);
+      fence_proxy_async_smem();
+    }
     __syncwarp();
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, 2 * L::QB);
@@ -303,6 +321,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
     }
     if (*abort_flag && lane == 0) {
       volatile int no_abort = 0;
+      mbar_wait(q_full, 0, &no_abort, p.err);
       for (int j = max(0, issued - STAGES); j < issued; ++j) {
         mbar_wait(&k_full[j % STAGES], (j / STAGES) & 1, &no_abort, p.err);
         mbar_wait(&v_full[j % STAGES], (j / STAGES) & 1, &no_abort, p.err);
@@ -323,6 +342,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
     const uint32_t sq = smem_u32(smem + L::OFF_Q);
     const uint32_t sones = smem_u32(smem + L::OFF_ONES);
     bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
+    fence_proxy_async_smem();   // Q scale words written by cp.async
     tc_fence_after();
     if (ok && leader) {
 #pragma unroll
