@@ -384,20 +384,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(st_free);
-      const float* l2v = lse2 + st * BQ + 32 * g;
-      const float* dv = dvec + st * BQ + 32 * g;
+      // LSE log2 e and D of this thread's 32 queries, four at a time (16-byte
+      // aligned rows)
+      const float4* l4 = reinterpret_cast<const float4*>(lse2 + st * BQ + 32 * g);
+      const float4* d4 = reinterpret_cast<const float4*>(dvec + st * BQ + 32 * g);
       const int qbase = q0 + 32 * g;
       float pmax = 0.f, dsmax = 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int q = qbase + i;
-        const bool valid = key < p.N && q < p.N && (!p.causal || key <= q);
-        const float pv = valid ? ex2_approx(fmaf(s[i], c, -l2v[i])) : 0.f;
-        const float ds = pv * (dp[i] - dv[i]);
-        s[i] = pv;
-        dp[i] = ds;
-        pmax = fmaxf(pmax, pv);
-        dsmax = fmaxf(dsmax, fabsf(ds));
+      for (int i4 = 0; i4 < 8; ++i4) {
+        const float4 la = l4[i4], da = d4[i4];
+        const float l2q[4] = {la.x, la.y, la.z, la.w}, dq4[4] = {da.x, da.y, da.z, da.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = 4 * i4 + e;
+          const int q = qbase + i;
+          const bool valid = key < p.N && q < p.N && (!p.causal || key <= q);
+          const float pv = valid ? ex2_approx(fmaf(s[i], c, -l2q[e])) : 0.f;
+          const float ds = pv * (dp[i] - dq4[e]);
+          s[i] = pv;
+          dp[i] = ds;
+          pmax = fmaxf(pmax, pv);
+          dsmax = fmaxf(dsmax, fabsf(ds));
+        }
       }
       // P and dS in blocks of 32 queries (this thread's columns)
       float inv;
