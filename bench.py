@@ -38,7 +38,7 @@ FP8_OVER_BF16 = 4.5 / 2.25
 # DRAM read + write of one fwd_fp4_kernel<128> launch on this workload, from the
 # ncu capture summarised in profiles/fwd_fp4_kernel_noncausal_4k.md (same kernel;
 # set to None whenever the kernel changes after the capture).
-FWD_FP4_TRAFFIC_BYTES = None
+FWD_FP4_TRAFFIC_BYTES = 71.61e6
 
 
 def peaks():
