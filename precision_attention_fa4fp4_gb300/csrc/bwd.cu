@@ -390,21 +390,44 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
       const float4* d4 = reinterpret_cast<const float4*>(dvec + st * BQ + 32 * g);
       const int qbase = q0 + 32 * g;
       float pmax = 0.f, dsmax = 0.f;
+      // every (key, query) of this warp's block in range and unmasked: the
+      // same arithmetic without the per-element validity test
+      const bool full = k0 + BK <= p.N && qbase + 32 <= p.N && (!p.causal || k0 + BK - 1 <= qbase);
+      if (full) {
 #pragma unroll
-      for (int i4 = 0; i4 < 8; ++i4) {
-        const float4 la = l4[i4], da = d4[i4];
-        const float l2q[4] = {la.x, la.y, la.z, la.w}, dq4[4] = {da.x, da.y, da.z, da.w};
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 la = l4[i4], da = d4[i4];
+          const float l2q[4] = {la.x, la.y, la.z, la.w}, dq4[4] = {da.x, da.y, da.z, da.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = 4 * i4 + e;
-          const int q = qbase + i;
-          const bool valid = key < p.N && q < p.N && (!p.causal || key <= q);
-          const float pv = valid ? ex2_approx(fmaf(s[i], c, -l2q[e])) : 0.f;
-          const float ds = pv * (dp[i] - dq4[e]);
-          s[i] = pv;
-          dp[i] = ds;
-          pmax = fmaxf(pmax, pv);
-          dsmax = fmaxf(dsmax, fabsf(ds));
+          for (int e = 0; e < 4; e += 2) {
+            const int i = 4 * i4 + e;
+            const float2 x = ffma2(make_float2(s[i], s[i + 1]), make_float2(c, c),
+                                   make_float2(-l2q[e], -l2q[e + 1]));
+            const float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            const float2 ds = fmul2(pv, fadd2(make_float2(dp[i], dp[i + 1]), make_float2(-dq4[e], -dq4[e + 1])));
+            s[i] = pv.x; s[i + 1] = pv.y;
+            dp[i] = ds.x; dp[i + 1] = ds.y;
+            pmax = fmax3(pmax, pv.x, pv.y);
+            dsmax = fmax3(dsmax, fabsf(ds.x), fabsf(ds.y));
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 la = l4[i4], da = d4[i4];
+          const float l2q[4] = {la.x, la.y, la.z, la.w}, dq4[4] = {da.x, da.y, da.z, da.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = 4 * i4 + e;
+            const int q = qbase + i;
+            const bool valid = key < p.N && q < p.N && (!p.causal || key <= q);
+            const float pv = valid ? ex2_approx(fmaf(s[i], c, -l2q[e])) : 0.f;
+            const float ds = pv * (dp[i] - dq4[e]);
+            s[i] = pv;
+            dp[i] = ds;
+            pmax = fmaxf(pmax, pv);
+            dsmax = fmaxf(dsmax, fabsf(ds));
+          }
         }
       }
       // P and dS in blocks of 32 queries (this thread's columns)
