@@ -1,6 +1,6 @@
 """Direct-P FP4 forward on the GPU vs the oracle on the same seeded inputs.
 
-Tolerance (the benchmark spec): rel-L2 <= 1e-3 and max-abs <= 1e-2 on O after
+Tolerance: rel-L2 <= 1e-3 and max-abs <= 1e-2 on O after
 the oracle's O is rounded to the kernel's output dtype; LSE to 1e-3 absolute.
 """
 import numpy as np
