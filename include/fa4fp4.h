@@ -210,7 +210,8 @@ FA4FP4_API fa4fp4_status fa4fp4_bwd_noalloc(
     float* dq, float* dk, float* dv, void* stream);
 
 /* BF16 FlashAttention forward, the speedup reference for fa4fp4_fwd
- * (technical summary, Results: "HAO's BF16 baseline").  q [B][Hq][N][d], k/v
+ * (technical summary, Results: the BF16 kernel its speedups are measured
+ * against).  q [B][Hq][N][d], k/v
  * [B][Hkv][N][d] bf16; exact online softmax with P rounded to bf16 for the
  * P V product.  o as in fa4fp4_fwd; lse (nullable) = natural-log LSE. */
 FA4FP4_API fa4fp4_status fa4bf16_fwd(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,

@@ -18,8 +18,8 @@
  *     magnitudes by classification instead of exp-then-round.
  *   - Methodology 1, "Consistent Normalization": the denominator is summed
  *     from the same rounded codes the P.V product consumes.
- *   - Methodology 1, "Format Selection": MXFP4 (power-of-two block scales over
- *     32-element fragments) for P and V; Q and K use MXFP4 here as well.
+ *   - Methodology 1, "Format Selection": MXFP4 (one power-of-two scale for every
+ *     32 consecutive elements) for P and V; Q and K use MXFP4 here as well.
  *   - Methodology 2, "Quantized Causal Backward": forward saves quantized Q/K,
  *     scales and the LSE; backward rebuilds P from them and uses FP8
  *     row/column views of Q, K, V for the gradient products.

@@ -4,8 +4,9 @@
 // summary, Methodology 2 ("Quantized Causal Backward"): the forward saves the
 // quantized Q/K payload, scales and the LSE; the backward rebuilds P from
 // them instead of a BF16 score path ("Reconstruction") and the gradient
-// products consume row/column-oriented FP8 views of Q, K, V ("Gradient
-// Formats"); the abstract adds FP8 gradient operands for P, dS and dO.
+// products read FP8 copies of Q, K and V blocked along whichever axis each
+// product contracts ("Gradient Formats"); the abstract adds FP8 gradient
+// operands for P, dS and dO.
 //
 // bwd_prep_kernel: D_i = sum_t dO_it O_it and zeroes dq (the main kernel
 //   adds into dq with bulk tensor reductions).  The MXFP8 views of dO come from the

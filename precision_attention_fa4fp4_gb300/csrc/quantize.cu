@@ -1,8 +1,10 @@
 // quantize.cu -- MXFP4 / MXFP8 block quantization (OCP MX rule).
 //
 // "Hardware-Aware FP4 FlashAttention-4", technical summary, Methodology 1
-// ("Format Selection": power-of-two block scales over 32-element fragments)
-// and Methodology 2 ("Gradient Formats": row/column-oriented FP8 views).
+// ("Format Selection": MXFP4, one scale that is a power of two for every 32
+// consecutive elements)
+// and Methodology 2 ("Gradient Formats": FP8 copies blocked along rows or
+// along columns).
 //
 // Per block of 32 values: amax, E8M0 exponent X = E(amax) - 127 - emax
 // (emax = 2 for E2M1, 8 for E4M3; clamped to [-127,127]), elements x*2^-X
