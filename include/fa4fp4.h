@@ -162,8 +162,9 @@ FA4FP4_API fa4fp4_status fa4fp4_fwd_nvfp4(const void* q_codes, const void* q_sca
 FA4FP4_API size_t fa4fp4_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
 
 /* Quantized causal backward (technical summary, Methodology 2 "Quantized
- * Causal Backward": P rebuilt from the saved quantized Q/K and the LSE;
- * row/column FP8 views of Q, K, V; abstract: FP8 gradient operands).
+ * Causal Backward": P recomputed from the forward's FP4 Q/K and its LSE;
+ * FP8 copies of Q, K and V blocked along each product's contraction axis;
+ * abstract: FP8 gradient operands).
  *   q4, k4: the forward's MXFP4 Q/K (along d);
  *   q8c, k8c: MXFP8 Q/K blocked along N ([B][H][d][Np] transposed views);
  *   v8r: MXFP8 V blocked along d ([B][Hkv][N][d]);

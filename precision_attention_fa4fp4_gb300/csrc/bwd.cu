@@ -1,9 +1,9 @@
 // bwd.cu -- quantized attention backward for sm_103a.
 //
 // "Hardware-Aware FP4 FlashAttention-4" (arXiv:2609.04105), technical
-// summary, Methodology 2 ("Quantized Causal Backward"): the forward saves the
-// quantized Q/K payload, scales and the LSE; the backward rebuilds P from
-// them instead of a BF16 score path ("Reconstruction") and the gradient
+// summary, Methodology 2 ("Quantized Causal Backward"): the forward keeps
+// the FP4 codes and block scales of Q and K and the log-sum-exp; the backward
+// recomputes P from those instead of a BF16 score path ("Reconstruction"), and the gradient
 // products read FP8 copies of Q, K and V blocked along whichever axis each
 // product contracts ("Gradient Formats"); the abstract adds FP8 gradient
 // operands for P, dS and dO.
