@@ -191,11 +191,12 @@ FA4FP4_API fa4fp4_status fa4fp4_bwd(const void* q4_codes, const void* q4_scales,
 /* Size of the fixed device scratch array used by fa4fp4_bwd_noalloc. */
 #define FA4FP4_BWD_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 
-/* fa4fp4_bwd for callers that cannot allocate device memory (inside a graph
- * capture that must not allocate, plugins whose host owns all allocations,
- * runtimes that forbid allocation after start-up).  The paper has no
- * counterpart: this is a deployment variant of fa4fp4_bwd.  Same arguments
- * and results as fa4fp4_bwd without the workspace; the scratch is a fixed
+/* fa4fp4_bwd for callers that cannot allocate device memory (plugins whose
+ * host framework owns every device allocation, runtimes that forbid
+ * allocation after start-up, code whose device memory is budgeted up front).
+ * The paper has no counterpart: this is a deployment variant of fa4fp4_bwd.
+ * Same arguments and results as fa4fp4_bwd without the workspace, and the
+ * same status for a bad argument; the scratch is a fixed
  * FA4FP4_BWD_NOALLOC_SCRATCH_BYTES device array inside this library (held by
  * every GPU that loads it until exit).  Returns FA4FP4_ERR_WORKSPACE when
  * fa4fp4_bwd_workspace_bytes(...) exceeds that size.  Allocates nothing.

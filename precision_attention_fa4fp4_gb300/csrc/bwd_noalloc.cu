@@ -1,9 +1,9 @@
 // bwd_noalloc.cu -- fa4fp4_bwd for callers that cannot allocate device memory.
 //
-// Some callers cannot call cudaMalloc: code running inside a CUDA-graph
-// capture that must not allocate, plugins whose host framework owns every
-// device allocation, or runtimes that forbid allocation after start-up.  For
-// them this file provides fa4fp4_bwd_noalloc, which runs the same backward as
+// Some callers cannot call cudaMalloc: plugins whose host framework owns every
+// device allocation, runtimes that forbid allocation after start-up, or code
+// whose device memory is budgeted once up front.  For them this file provides
+// fa4fp4_bwd_noalloc, which runs the same backward as
 // fa4fp4_bwd but takes its scratch (the MXFP8 views of dO and the row sums D)
 // from a fixed array in device memory instead of a caller workspace.
 //
@@ -50,13 +50,19 @@ extern "C" fa4fp4_status fa4fp4_bwd_noalloc(
     const void* v8r_codes, const void* v8r_scales, const void* o, int o_dtype, const void* dout,
     const float* lse, int B, int Hq, int Hkv, int N, int d, float softmax_scale, int causal,
     float* dq, float* dk, float* dv, void* stream) {
-  const size_t need = fa4fp4_bwd_workspace_bytes(B, Hq, Hkv, N, d);
-  if (need > kScratchBytes) return FA4FP4_ERR_WORKSPACE;
-  void* scratch = nullptr;
-  if (need > 0) {
-    scratch = scratch_address();
-    if (!scratch) return FA4FP4_ERR_CUDA;
-  }
+  // The arguments are checked first, by fa4fp4_bwd itself: given no
+  // workspace it validates every argument, launches nothing, and returns
+  // FA4FP4_ERR_WORKSPACE for a well-formed non-empty problem.  So a bad
+  // argument gets the same status from both entry points, and the scratch
+  // address is looked up only for a call that will run.
+  const fa4fp4_status s =
+      fa4fp4_bwd(q4_codes, q4_scales, k4_codes, k4_scales, q8c_codes, q8c_scales, k8c_codes, k8c_scales,
+                 v8r_codes, v8r_scales, o, o_dtype, dout, lse, B, Hq, Hkv, N, d, softmax_scale, causal, dq,
+                 dk, dv, nullptr, 0, stream);
+  if (s != FA4FP4_ERR_WORKSPACE) return s;   // an argument error, or an empty problem (OK)
+  if (fa4fp4_bwd_workspace_bytes(B, Hq, Hkv, N, d) > kScratchBytes) return FA4FP4_ERR_WORKSPACE;
+  void* scratch = scratch_address();
+  if (!scratch) return FA4FP4_ERR_CUDA;
   return fa4fp4_bwd(q4_codes, q4_scales, k4_codes, k4_scales, q8c_codes, q8c_scales, k8c_codes,
                     k8c_scales, v8r_codes, v8r_scales, o, o_dtype, dout, lse, B, Hq, Hkv, N, d,
                     softmax_scale, causal, dq, dk, dv, scratch, kScratchBytes, stream);

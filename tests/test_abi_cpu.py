@@ -124,3 +124,25 @@ def test_empty_problems_are_noops(lib):
     assert lib.fa4fp4_bwd(*([null] * 11), 0, null, null, 0, 4, 2, 300, 64, 0.0, 1,
                           null, null, null, null, 0, null) == UNSUP
     assert lib.fa4fp4_quantize_qkv(null, null, null, -1, 4, 2, 64, 128, *n6, null) == INVALID
+
+
+def test_noalloc_validates_like_bwd(lib):
+    """A problem too large for the fixed scratch array still gets the same
+    argument errors from fa4fp4_bwd_noalloc as from fa4fp4_bwd (validation
+    comes first; nothing is launched)."""
+    p, null = ctypes.c_void_p(4096), None
+    INVALID, UNSUP, WORKSPACE = 1, 2, 6
+    bwd_na = lib.fa4fp4_bwd_noalloc
+    bwd_na.restype = ctypes.c_int
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    bwd_na.argtypes = [vp] * 11 + [i, vp, vp, i, i, i, i, i, f, i, vp, vp, vp, vp]
+    B, Hq, Hkv, N = 2, 32, 8, 8192
+    assert lib.fa4fp4_bwd_workspace_bytes(B, Hq, Hkv, N, 128) > (16 << 20)
+    for odt, d, want in ((7, 128, INVALID), (0, 96, UNSUP)):
+        got_na = bwd_na(*([p] * 11), odt, p, p, B, Hq, Hkv, N, d, 0.0, 1, p, p, p, null)
+        got = lib.fa4fp4_bwd(*([p] * 11), odt, p, p, B, Hq, Hkv, N, d, 0.0, 1, p, p, p, p, 1 << 40, null)
+        assert got_na == got == want
+    # null gradient pointers: invalid from both
+    assert bwd_na(*([p] * 11), 0, p, p, B, Hq, Hkv, N, 128, 0.0, 1, null, p, p, null) == INVALID
+    # well-formed but oversized: the scratch limit
+    assert bwd_na(*([p] * 11), 0, p, p, B, Hq, Hkv, N, 128, 0.0, 1, p, p, p, null) == WORKSPACE

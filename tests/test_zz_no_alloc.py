@@ -1,6 +1,6 @@
 """fa4fp4_bwd_noalloc: the backward for callers that cannot allocate device
-memory (graph captures that must not allocate, plugins whose host owns every
-device allocation).  It must give the same gradients as fa4fp4_bwd with a
+memory (plugins whose host framework owns every device allocation, runtimes
+that forbid allocation after start-up).  It must give the same gradients as fa4fp4_bwd with a
 caller workspace, call after call, although every call reuses the same fixed
 scratch array inside the library.
 
