@@ -1,9 +1,10 @@
 """NVFP4 Q/K on the GPU vs the oracle.
 
 Quantization: codes, E4M3 block scales and the FP32 tensor scale bit-exact.
-Forward: the oracle runs on the E2M1 x E4M3 values without the tensor scales
-(exact in FP32) with the softmax scale fl32(fl32(scale * ts_q) * ts_k), which
-is how the kernel folds the tensor scales; tolerances as for the MXFP4 forward.
+Forward: the oracle runs on the plain definition, deq = E2M1 x E4M3 x the
+FP32 tensor scale, with the softmax scale 1/sqrt(d).  (The kernel folds the
+two tensor scales into the softmax scale; the CPU tests pin that this moves
+O and LSE by FP32 rounding only.)  Tolerances as for the MXFP4 forward.
 """
 import numpy as np
 import pytest
@@ -52,14 +53,12 @@ def check(w: Workload, fp8pv: bool, out_bf16=False, rows=None, seed=0):
     qf, kf, vf = (t.float().numpy() for t in (q, k, v))
     cq, sq, tq = oracle.quantize_nvfp4(qf)
     ck, sk, tk = oracle.quantize_nvfp4(kf)
-    Qu = oracle.dequantize_nvfp4(cq, sq, 1.0, qf.shape)       # exact in FP32
-    Ku = oracle.dequantize_nvfp4(ck, sk, 1.0, kf.shape)
+    Qd = oracle.dequantize_nvfp4(cq, sq, tq, qf.shape)
+    Kd = oracle.dequantize_nvfp4(ck, sk, tk, kf.shape)
     fmt = 1 if fp8pv else 0
     Vd = oracle.dequantize(*oracle.quantize(vf, fmt, 1), vf.shape, fmt, 1)
-    s0 = np.float32(1.0 / np.sqrt(w.d))
-    scale = np.float32(np.float32(s0 * np.float32(tq)) * np.float32(tk))
     rows = np.arange(w.B * w.Hq * w.N) if rows is None else np.asarray(rows)
-    Oo, Lo = oracle.fwd(Qu, Ku, Vd, softmax_scale=float(scale), causal=w.causal, rows=rows, mode=2 if fp8pv else 0)
+    Oo, Lo = oracle.fwd(Qd, Kd, Vd, causal=w.causal, rows=rows, mode=2 if fp8pv else 0)
     name = w.name + (" NVFP4 Q/K + FP8 P/V" if fp8pv else " NVFP4 Q/K")
     assert_close(o.reshape(-1, w.d)[rows], round_like(Oo, out_bf16), name + " O")
     assert np.max(np.abs(lse.reshape(-1)[rows] - Lo)) < 1e-3, name + " LSE"

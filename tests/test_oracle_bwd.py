@@ -140,3 +140,83 @@ def test_mode0_within_fp8_bound():
     for a, b in zip(g0, g1):
         rel = np.linalg.norm(a - b) / np.linalg.norm(b)
         assert 1e-4 < rel < 0.06
+
+
+# ---------------------------------------------------------------------------
+# The MXFP8 block axes of the quantized backward (Methodology 2, "Gradient
+# Formats": row- and column-oriented FP8 views; the block runs along the
+# contraction axis of the product each operand feeds).  In every case below
+# one operand holds a value 2^-20 of its neighbour along the WRONG axis and
+# equal values along the stated one: blocked along the stated axis it is
+# exact, blocked along the other it shares an E8M0 scale with a value 2^20
+# larger and flushes to zero (E4M3's smallest subnormal is 2^-9 of the
+# block's scale, and the scale puts the block maximum in [256, 512)).  The
+# expected gradients are written out by hand; softmax_scale = fl32(ln 2)
+# makes c = 1, so P = 2^s exactly with LSE = 0.
+# ---------------------------------------------------------------------------
+
+AX_N, AX_D = 64, 64
+TINY = 2.0 ** -20
+
+
+def axis_case(which):
+    N, d = AX_N, AX_D
+    z = lambda: np.zeros((1, 1, N, d), np.float32)
+    Q4, K4, Q8, K8, V8, O, dO = z(), z(), z(), z(), z(), z(), z()
+    LSE = np.zeros((1, 1, N), np.float32)
+    if which == "P_along_queries":
+        # s_i,n = a_n: P_i,0 = 1, P_i,1 = 2^-20, P = 0 for n >= 2 (equal down
+        # each key's column of queries, 2^20 apart along a query's row)
+        Q4[..., 0] = 1.0
+        K4[0, 0, :, 0] = -200.0
+        K4[0, 0, 0, 0], K4[0, 0, 1, 0] = 0.0, -20.0
+        dO[:] = 1.0
+    elif which == "dO_for_dV_along_queries":
+        # P = 1; dO_i = (1, 2^-20, 0, ...) for every query i
+        dO[..., 0], dO[..., 1] = 1.0, TINY
+    elif which == "dO_for_dP_along_d_and_dS_for_dQ_along_keys":
+        # P = 1, D = 0; dO row 1 = 2^-20 * ones, every other row ones; V = ones:
+        # dP_1,n = 64 * 2^-20 for every key (equal along the row), 2^20 below
+        # row 0 down each column
+        dO[:] = 1.0
+        dO[0, 0, 1] = TINY
+        V8[:] = 1.0
+        K8[:] = 1.0
+    elif which == "dS_for_dK_along_queries":
+        # P = 1, D = 0; dO = ones; V_0 = ones, V_1 = 2^-20 * ones: dS_i,1 =
+        # 2^-14 for every query (equal down the column), 2^20 below dS_i,0
+        dO[:] = 1.0
+        V8[0, 0, 0] = 1.0
+        V8[0, 0, 1] = TINY
+        Q8[:] = 1.0
+    return Q4, K4, Q8, K8, V8, O, dO, LSE
+
+
+SCALE_C1 = float(np.float32(np.log(2.0)))
+
+
+@pytest.mark.parametrize("which", ["P_along_queries", "dO_for_dV_along_queries",
+                                   "dO_for_dP_along_d_and_dS_for_dQ_along_keys", "dS_for_dK_along_queries"])
+def test_mxfp8_block_axes(which):
+    args = axis_case(which)
+    dQ, dK, dV = oracle.bwd(*args, softmax_scale=SCALE_C1, causal=False, mode=0)
+    N, d = AX_N, AX_D
+    ones = np.ones(d)
+    if which == "P_along_queries":
+        # dV_n = sum_i P_i,n dO_i: key 0 -> 64, key 1 -> 64 * 2^-20
+        np.testing.assert_array_equal(dV[0], 64 * ones)
+        np.testing.assert_array_equal(dV[1], 64 * TINY * ones)
+        np.testing.assert_array_equal(dV[2:], 0)
+    elif which == "dO_for_dV_along_queries":
+        want = np.zeros(d)
+        want[0], want[1] = 64.0, 64 * TINY
+        np.testing.assert_array_equal(dV, np.broadcast_to(want, dV.shape))
+    elif which == "dO_for_dP_along_d_and_dS_for_dQ_along_keys":
+        # dQ_1 = scale * sum_n dS_1,n K_n = scale * 64 keys * 64 * 2^-20
+        np.testing.assert_array_equal(dQ[1], SCALE_C1 * 64 * 64 * TINY * ones)
+        np.testing.assert_array_equal(dQ[0], SCALE_C1 * 64 * 64 * ones)
+    elif which == "dS_for_dK_along_queries":
+        # dK_1 = scale * sum_i dS_i,1 Q_i = scale * 64 queries * 2^-14
+        np.testing.assert_array_equal(dK[1], SCALE_C1 * 64 * 64 * TINY * ones)
+        np.testing.assert_array_equal(dK[0], SCALE_C1 * 64 * 64 * ones)
+        np.testing.assert_array_equal(dK[2:], 0)

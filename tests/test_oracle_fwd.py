@@ -267,3 +267,55 @@ def test_nvfp4_qk_scores_beat_mxfp4_on_outlier_channels():
     e_mx = np.linalg.norm(mx - S) / np.linalg.norm(S)
     e_nv = np.linalg.norm(nv - S) / np.linalg.norm(S)
     assert e_nv < e_mx, (e_nv, e_mx)
+
+
+@pytest.mark.parametrize("N", [1, 77, 300])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hq,Hkv", [(2, 2), (6, 2)])
+def test_attention_fp64_equals_brute_force(N, causal, Hq, Hkv):
+    """The unquantized FP64 reference (used for the error report and the BF16
+    kernel's parity) is textbook softmax attention: it equals the numpy brute
+    force to 1e-12, with the causal mask and GQA head sharing."""
+    d = 64
+    Q, K, V = rand((2, Hq, N, d), 41, 2.0), rand((2, Hkv, N, d), 42, 2.0), rand((2, Hkv, N, d), 43)
+    O = oracle.attention_fp64(Q, K, V, causal=causal)
+    Ob, _ = brute_softmax_attention(Q, K, V, 1 / np.sqrt(d), causal)
+    np.testing.assert_allclose(O, Ob.reshape(-1, d), rtol=0, atol=1e-12)
+    # an explicit softmax scale and a row subset
+    rows = np.array([0, N - 1, Hq * N + N // 2])
+    O2 = oracle.attention_fp64(Q, K, V, softmax_scale=0.3, causal=causal, rows=rows)
+    Ob2, _ = brute_softmax_attention(Q, K, V, np.float32(0.3), causal)
+    np.testing.assert_allclose(O2, Ob2.reshape(-1, d)[rows], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", [0, 2])
+@pytest.mark.parametrize("N,d,causal,outliers", [(300, 64, True, 0), (1000, 128, False, 0), (700, 128, False, 4)])
+def test_nvfp4_folded_tensor_scales_match_plain_definition(N, d, causal, outliers, mode):
+    """NVFP4 Q/K by the plain definition: s = fl32(deq(Q).deq(K)) with the
+    FP32 tensor scales inside deq, softmax scale 1/sqrt(d).  Folding the two
+    tensor scales into the softmax scale instead, fl32(fl32(scale*ts_q)*ts_k)
+    on scores of the E2M1 x E4M3 values alone, moves the scores by FP32
+    rounding only; O and LSE stay within the parity bar (rel-L2 1e-3,
+    max-abs 1e-2, LSE 1e-3) of the plain form, for Direct-P and the FP8 P/V
+    route."""
+    from precision_attention_fa4fp4_gb300.inputs import Workload, make_inputs
+    w = Workload("nv_fold", 1, 4, 2, N, d, causal=causal, n_outliers=outliers)
+    q, k, v = (t.float().numpy() for t in make_inputs(w, seed=5))
+    cq, sq, tq = oracle.quantize_nvfp4(q)
+    ck, sk, tk = oracle.quantize_nvfp4(k)
+    fmt = 1 if mode == 2 else 0
+    Vd = oracle.dequantize(*oracle.quantize(v, fmt, 1), v.shape, fmt, 1)
+    # plain definition
+    Qt, Kt = oracle.dequantize_nvfp4(cq, sq, tq, q.shape), oracle.dequantize_nvfp4(ck, sk, tk, k.shape)
+    Op, Lp = oracle.fwd(Qt, Kt, Vd, causal=causal, mode=mode)
+    # folded form
+    Qu, Ku = oracle.dequantize_nvfp4(cq, sq, 1.0, q.shape), oracle.dequantize_nvfp4(ck, sk, 1.0, k.shape)
+    s0 = np.float32(1 / np.sqrt(d))
+    folded = np.float32(np.float32(s0 * np.float32(tq)) * np.float32(tk))
+    Of, Lf = oracle.fwd(Qu, Ku, Vd, softmax_scale=float(folded), causal=causal, mode=mode)
+    rel = np.linalg.norm(Of - Op) / np.linalg.norm(Op)
+    assert rel <= 1e-3 and np.max(np.abs(Of - Op)) <= 1e-2 and np.max(np.abs(Lf - Lp)) <= 1e-3
+    # the tensor scales are really inside the plain scores (a dropped ts would
+    # shift every LSE by orders of magnitude of the logit scale)
+    Ox, Lx = oracle.fwd(Qu, Ku, Vd, causal=causal, mode=mode)
+    assert np.max(np.abs(Lx - Lp)) > 0.05
