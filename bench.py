@@ -8,8 +8,11 @@ L2 is flushed (a 256 MiB write) before every timed step; each step is timed
 with CUDA events on the launching stream.
 
 Also reported: the forward kernel alone (the roofline line), the BF16 kernel on
-the same inputs, the causal GQA training config (forward + backward) and an
-end-to-end figure through host buffers.
+the same inputs, the quantize launch against HBM bandwidth, the causal GQA
+training config (forward + backward, with roofline fractions), the video-DiT
+and sweep workloads (TFLOP/s and roofline fraction per point), each forward
+path's error against FP64 softmax attention on sampled rows of every workload
+and on extreme-logit inputs, and an end-to-end figure through host buffers.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 Under torchrun every rank runs its own copy of the workload (independent
@@ -35,10 +38,28 @@ from precision_attention_fa4fp4_gb300.inputs import FWD_4K, SWEEP, TRAIN_8B, VID
 METRIC = "FP4 attention fwd TFLOP/s (noncausal, d=128) and speedup vs own BF16 kernel"
 FP4_OVER_BF16 = 13.5 / 2.25     # nominal dense FP4 : BF16 tensor rate on GB300
 FP8_OVER_BF16 = 4.5 / 2.25
-# DRAM read + write of one fwd_fp4_kernel<128> launch on this workload, from the
-# ncu capture summarised in profiles/fwd_fp4_kernel_noncausal_4k.md (same kernel;
-# set to None whenever the kernel changes after the capture).
-FWD_FP4_TRAFFIC_BYTES = 71.61e6
+# DRAM read + write of one fwd_fp4_kernel<128> launch on the 4K workload, from
+# one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), with the
+# SHA-256 of the kernel's source files at that capture.  The figure is
+# reported only while those files are unchanged; after any edit it reads null
+# until the kernel is captured again.
+FWD_FP4_TRAFFIC = {"bytes": None, "sources_sha256": None}
+FWD_FP4_SOURCES = ("csrc/fwd_fp4.cu", "csrc/common.cuh", "csrc/internal.h")
+
+
+def fwd_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in FWD_FP4_SOURCES:
+        with open(os.path.join(ROOT, "precision_attention_fa4fp4_gb300", rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def fwd_traffic_bytes():
+    if FWD_FP4_TRAFFIC["bytes"] is None or FWD_FP4_TRAFFIC["sources_sha256"] != fwd_sources_sha256():
+        return None
+    return FWD_FP4_TRAFFIC["bytes"]
 
 
 def peaks():
@@ -153,7 +174,10 @@ class Flusher:
 
 
 def time_steps(step, warmup, steps, flush, world, inner=None):
-    """Returns (per-step ms list, per-step inner-kernel ms list or None)."""
+    """Returns (per-step ms list, per-step inner-kernel ms list or None).  With
+    `inner`, the step gets three events: it records [2] before its first
+    launch, [0] and [1] around the inner kernel; the per-step time of the
+    launches before the inner kernel ([2] to [0]) is kept in time_steps.pre."""
     for _ in range(warmup):
         flush()
         step(None)
@@ -163,16 +187,18 @@ def time_steps(step, warmup, steps, flush, world, inner=None):
     for _ in range(steps):
         flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ie = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] if inner else None
+        ie = [torch.cuda.Event(enable_timing=True) for _ in range(3)] if inner else None
         e0.record()
         step(ie)
         e1.record()
         evs.append((e0, e1, ie))
     barrier(world)
+    time_steps.pre = []
     for e0, e1, ie in evs:
         outer.append(e0.elapsed_time(e1))
         if ie:
             inner_ms.append(ie[0].elapsed_time(ie[1]))
+            time_steps.pre.append(ie[2].elapsed_time(ie[0]))
     return outer, (inner_ms if inner else None)
 
 
@@ -191,6 +217,8 @@ def run_ours(args, rank, world, local):
     flush = Flusher(dev)
 
     def step(ie):
+        if ie:
+            ie[2].record()
         fa.quantize_qkv(q, k, v, out=(q4, k4, vt))
         if ie:
             ie[0].record()
@@ -214,6 +242,11 @@ def run_ours(args, rank, world, local):
     flops = w.fwd_flops
     ms = max_over_ranks(statistics.mean(step_ms), world)
     fwd_mean = max_over_ranks(statistics.mean(fwd_ms), world)
+    quant_mean = max_over_ranks(statistics.mean(time_steps.pre), world)
+    # algorithmic HBM bytes of the quantize launch: bf16 Q, K, V read; E2M1
+    # codes (half a byte per element) and one E8M0 byte per 32 elements written
+    nel = q.numel() + k.numel() + v.numel()
+    quant_bytes = 2 * nel + nel // 2 + nel // 32
 
     # kernel-only forward (L2 flushed) and the BF16 denominator
     fwd_only, _ = time_steps(step_fwd_only, args.warmup, args.steps, flush, world)
@@ -302,16 +335,35 @@ def run_ours(args, rank, world, local):
     except Exception as e:  # reported, not hidden
         train = {"error": f"{type(e).__name__}: {e}"}
 
+    pk = peaks()
+    fp4_peak = pk["bf16"] * FP4_OVER_BF16
+    if isinstance(train, dict):
+        if "fwd_tflops" in train:
+            train["fwd_frac"] = round(train["fwd_tflops"] / fp4_peak, 4)
+        if "fwd_fp8pv_tflops" in train:
+            train["fwd_fp8pv_frac"] = round(train["fwd_fp8pv_tflops"] / (pk["bf16"] * FP8_OVER_BF16), 4)
+        if "bwd_tflops" in train:
+            train["bwd_frac"] = round(train["bwd_tflops"] / (pk["bf16"] * FP8_OVER_BF16), 4)
+            train["bwd_peak"] = round(pk["bf16"] * FP8_OVER_BF16, 1)
+
     workloads = None
     if not args.no_sweep:
         try:
             workloads = run_workloads(fa, dev, 3)
+            for row in workloads:
+                row["fp4_frac"] = round(row["fp4_tflops"] / fp4_peak, 4)
+                row["bf16_frac"] = round(row["bf16_tflops"] / pk["bf16"], 4)
         except Exception as e:
             workloads = {"error": f"{type(e).__name__}: {e}"}
     clock_info = clocks.stop() if clocks else None
 
-    pk = peaks()
-    fp4_peak = pk["bf16"] * FP4_OVER_BF16
+    accuracy = None
+    if not args.no_accuracy:
+        try:
+            accuracy = accuracy_report(fa, dev)
+        except Exception as e:
+            accuracy = {"error": f"{type(e).__name__}: {e}"}
+
     achieved = flops / (fwd_mean * 1e-3) / 1e12
     result = {
         "metric": METRIC,
@@ -334,10 +386,15 @@ def run_ours(args, rank, world, local):
         "speedup_vs_bf16_kernel_only": round(bf16_mean / fwd_only_ms, 3),
         "fwd_kernel_tflops": round(flops / (fwd_only_ms * 1e-3) / 1e12, 2),
         "bf16_kernel_tflops": round(flops / (bf16_mean * 1e-3) / 1e12, 2),
-        "quantize_ms": round(ms - fwd_mean, 4),
+        "quantize_ms": round(quant_mean, 4),
+        "quantize_roofline": {"kernel": "quant_qkv_kernel", "bound": "hbm",
+                              "achieved": round(quant_bytes / (quant_mean * 1e-3) / 1e9, 1),
+                              "peak": pk["hbm"], "unit": "GB/s",
+                              "frac": round(quant_bytes / (quant_mean * 1e-3) / 1e9 / pk["hbm"], 4),
+                              "algorithmic_bytes": quant_bytes},
         "roofline": {"kernel": "fwd_fp4_kernel<128>", "bound": "tensor", "achieved": round(achieved, 1),
                      "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 4),
-                     "traffic": FWD_FP4_TRAFFIC_BYTES,
+                     "traffic": fwd_traffic_bytes(),
                      "peak_source": f"{pk['source']} bf16 burst {pk['bf16']} TFLOP/s x nominal FP4/BF16 ratio 6"},
         "e2e": {"value": round(whole_job_tflops(flops, world, e2e_mean), 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_mean, 4),
@@ -348,8 +405,85 @@ def run_ours(args, rank, world, local):
         "clocks": clock_info,
         "train": train,
         "workloads": workloads,
+        "accuracy": accuracy,
     }
     return result
+
+
+# ----------------------------------------------------------------------------
+# error against unquantized FP64 attention (reported, not gated)
+# ----------------------------------------------------------------------------
+def fp64_attention_rows(q, k, v, rows, causal):
+    """Textbook softmax(QK^T/sqrt(d))V in FP64 on the host for the selected
+    query rows ((b*Hq+h)*N+i) of the raw bf16 inputs (K/V head h/(Hq/Hkv))."""
+    B, Hq, N, d = q.shape
+    group = Hq // k.shape[1]
+    rows = torch.as_tensor(rows, dtype=torch.int64)
+    out = torch.empty((len(rows), d), dtype=torch.float64)
+    bh = rows // N
+    for u in torch.unique(bh).tolist():
+        sel = (bh == u).nonzero().flatten()
+        b, h = divmod(u, Hq)
+        i = rows[sel] % N
+        kk = k[b, h // group].double()
+        s = (q[b, h, i].double() @ kk.T) / (d ** 0.5)
+        if causal:
+            s = s.masked_fill(torch.arange(N).view(1, N) > i.view(-1, 1), float("-inf"))
+        out[sel] = torch.softmax(s, dim=-1) @ v[b, h // group].double()
+    return out
+
+
+def error_vs_fp64(o, ref):
+    o = o.double()
+    rel = float(torch.linalg.norm(o - ref) / torch.linalg.norm(ref))
+    cos = torch.nn.functional.cosine_similarity(o, ref, dim=1)
+    return {"rel_l2": round(rel, 5), "cosine": round(float(cos.mean()), 5)}
+
+
+def accuracy_report(fa, dev):
+    """Each forward path's output (FP32) on sampled rows of every workload
+    against FP64 softmax attention on the same raw bf16 inputs."""
+    from precision_attention_fa4fp4_gb300.inputs import TINY, extreme_logit_inputs, sample_rows
+    cases = [(TINY, None), (FWD_4K, [0, 63]), (VIDEO_DIT, [0, 23]), (SWEEP[0], [0]), (SWEEP[11], [63]),
+             (TRAIN_8B, [0, 37])]
+    report = []
+    for w, heads in cases + [("extreme_logits", False), ("extreme_logits", True)]:
+        if w == "extreme_logits":
+            causal = heads
+            q, k, v = extreme_logit_inputs()
+            name, rows = f"extreme_logits_n640_d128{'_causal' if causal else ''}", torch.arange(q.numel() // q.shape[-1])
+        else:
+            causal = w.causal
+            q, k, v = make_inputs(w, seed=0)
+            name = w.name
+            rows = (torch.arange(w.B * w.Hq * w.N) if heads is None
+                    else sample_rows(w, tiles_per_head=2, heads=heads))
+        ref = fp64_attention_rows(q, k, v, rows, causal)
+        qd, kd, vd = (t.to(dev) for t in (q, k, v))
+        d = q.shape[-1]
+        q4, k4 = fa.quantize(qd), fa.quantize(kd)
+        vt = fa.quantize(vd, fa.FMT_MXFP4, fa.ALONG_N)
+        o, _ = fa.fwd(q4, k4, vt, causal=causal, out_dtype=fa.OUT_F32)
+        row = {"workload": name, "rows": len(rows),
+               "directp": error_vs_fp64(o.reshape(-1, d)[rows.to(dev)].cpu(), ref)}
+        del o
+        v8 = fa.quantize(vd, fa.FMT_MXFP8, fa.ALONG_N)
+        o, _ = fa.fwd_fp8pv(q4, k4, v8, causal=causal, out_dtype=fa.OUT_F32)
+        row["fp8pv"] = error_vs_fp64(o.reshape(-1, d)[rows.to(dev)].cpu(), ref)
+        del o, v8
+        qn, kn = fa.quantize_nvfp4(qd), fa.quantize_nvfp4(kd)
+        o, _ = fa.fwd_nvfp4(qn, kn, vt, causal=causal, out_dtype=fa.OUT_F32)
+        row["nvfp4_qk"] = error_vs_fp64(o.reshape(-1, d)[rows.to(dev)].cpu(), ref)
+        del o, qn, kn
+        o, _ = fa.bf16_fwd(qd, kd, vd, causal=causal, out_dtype=fa.OUT_F32)
+        row["bf16"] = error_vs_fp64(o.reshape(-1, d)[rows.to(dev)].cpu(), ref)
+        fa.sync_status()
+        report.append(row)
+        del o, q4, k4, vt, qd, kd, vd
+        torch.cuda.empty_cache()
+    return {"reference": "FP64 softmax attention on the raw bf16 inputs (host); rel-L2 over the sampled rows, "
+                         "mean cosine per row; every path with FP32 output",
+            "rows": report}
 
 
 def run_workloads(fa, dev, steps):
@@ -457,11 +591,32 @@ def oracle_sample(heads: int = 8, rows_tiles: int = 32):
     return dt, flops, oracle.num_threads()
 
 
+def oracle_tiny_full():
+    """The tiny workload (B1 H2 N256 d64) in full: oracle quantize of Q/K/V
+    and the Direct-P forward of every row.  Returns (seconds, flops)."""
+    import oracle
+    from precision_attention_fa4fp4_gb300.inputs import TINY
+    q, k, v = (t.float().numpy() for t in make_inputs(TINY, seed=0))
+    oracle.build()
+    reps = 20
+    t0 = time.time()
+    for _ in range(reps):
+        Qd = oracle.dequantize(*oracle.quantize(q, 0, 0), q.shape, 0, 0)
+        Kd = oracle.dequantize(*oracle.quantize(k, 0, 0), k.shape, 0, 0)
+        Vd = oracle.dequantize(*oracle.quantize(v, 0, 1), v.shape, 0, 1)
+        oracle.fwd(Qd, Kd, Vd)
+    return (time.time() - t0) / reps, TINY.fwd_flops
+
+
 def cpu_baseline_entry():
     dt, flops, thr = oracle_sample(heads=8, rows_tiles=32)
+    tdt, tflops = oracle_tiny_full()
     return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
             "sample": "4K workload, 8 heads of batch 0: oracle MXFP4 quantize of Q/K/V and the Direct-P "
-                      f"forward of all 4096 query rows of each ({flops / 1e9:.1f} GFLOP in {dt:.1f} s)"}
+                      f"forward of all 4096 query rows of each ({flops / 1e9:.1f} GFLOP in {dt:.1f} s)",
+            "tiny_full": {"workload": "tiny_b1_h2_n256_d64", "ms": round(tdt * 1e3, 3),
+                          "tflops": round(tflops / tdt / 1e12, 6),
+                          "what": "whole workload: quantize Q/K/V + Direct-P forward, mean of 20 runs"}}
 
 
 def run_reference(args, rank, world):
@@ -496,6 +651,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the per-workload kernel table")
+    ap.add_argument("--no-accuracy", action="store_true", help="skip the error report against FP64 attention")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":

@@ -96,3 +96,16 @@ def sample_rows(w: Workload, tiles_per_head: int = 8, heads=None, seed: int = 1)
             lo, hi = t * 128, min(w.N, t * 128 + 128)
             rows.extend(bh * w.N + i for i in range(lo, hi))
     return torch.tensor(rows, dtype=torch.int64)
+
+
+def extreme_logit_inputs(N: int = 640, d: int = 128, seed: int = 3):
+    """Synthetic inputs whose scaled logits reach several hundred (far above
+    500): Q and K N(0, 36), K's 128-key tile t multiplied by t + 1, so every
+    later key tile raises the row maximum by a large step; V N(0, 1).
+    bf16 CPU tensors [1, 2, N, d]."""
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(1, 2, N, d, generator=g) * 6.0
+    k = torch.randn(1, 2, N, d, generator=g) * 6.0
+    k = k * (1.0 + torch.arange(N).float().div(128).floor().view(1, 1, N, 1))
+    v = torch.randn(1, 2, N, d, generator=g)
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)

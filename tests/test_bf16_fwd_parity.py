@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 from gpu_util import assert_close, require_gpu
-from precision_attention_fa4fp4_gb300.inputs import FWD_4K, TINY, TRAIN_8B, Workload, make_inputs, sample_rows
+from precision_attention_fa4fp4_gb300.inputs import FWD_4K, SWEEP, TINY, TRAIN_8B, VIDEO_DIT, Workload, make_inputs, sample_rows
 
 pytestmark = pytest.mark.gpu
 TOL = 3e-3
@@ -46,3 +46,13 @@ def test_4k_sampled():
 
 def test_train_causal_gqa_sampled():
     check(TRAIN_8B, rows=sample_rows(TRAIN_8B, tiles_per_head=3, heads=[5]))
+
+
+def test_video_dit_sampled():
+    """Outlier channels (logit std ~11): peaked rows, ragged N = 32760."""
+    check(VIDEO_DIT, rows=sample_rows(VIDEO_DIT, tiles_per_head=3, heads=[0, 23]))
+
+
+@pytest.mark.parametrize("w", [SWEEP[0], SWEEP[5], SWEEP[11]], ids=lambda w: w.name)
+def test_sweep_points_sampled(w):
+    check(w, rows=sample_rows(w, tiles_per_head=2, heads=[w.B * w.Hq - 1]))

@@ -86,6 +86,20 @@ def test_train_causal_gqa_sampled():
     check(w, qrows=qrows, krows=krows, heads_for_fwd=heads)
 
 
+def test_train_causal_gqa_sampled_middle_tile_other_batch():
+    """The same shape on batch 0, kv head 2: dK/dV on a middle key tile (keys
+    4096-4223, half the queries above the diagonal), dQ on a middle and the
+    last query tile of the group's third query head."""
+    w = TRAIN_8B
+    b, hk = 0, 2
+    heads = [b * w.Hq + hk * 4 + u for u in range(4)]
+    kbase = (b * w.Hkv + hk) * w.N
+    krows = kbase + np.arange(4096, 4224)
+    qbase = heads[2] * w.N
+    qrows = np.concatenate([qbase + np.arange(2560, 2688), qbase + np.arange(w.N - 128, w.N)])
+    check(w, qrows=qrows, krows=krows, heads_for_fwd=heads)
+
+
 def test_causal_gqa_partial_cta_group():
     """Six (batch, kv head) pairs: the causal backward orders its CTAs in groups
     of four pairs, so the last group holds two; ragged N (three key tiles)."""

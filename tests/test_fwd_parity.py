@@ -73,9 +73,35 @@ def test_video_dit_sampled():
     check(VIDEO_DIT, False, rows=sample_rows(VIDEO_DIT, tiles_per_head=4, heads=[0, 23]))
 
 
+def check_heads(w: Workload, bh_list, tiles_per_head=3, out_bf16=True, seed=0):
+    """The GPU runs the whole problem; the oracle quantizes and runs only the
+    sampled (batch, head) pairs of an MHA workload (heads are independent
+    problems), on `tiles_per_head` query tiles of each, first and last
+    included."""
+    assert w.Hq == w.Hkv
+    fa = require_gpu()
+    q, k, v = make_inputs(w, seed=seed)
+    o, lse = gpu_fwd(fa, q, k, v, w.causal, out_bf16)
+    sel = lambda t: t.reshape(w.B * w.Hq, w.N, w.d)[bh_list].reshape(1, len(bh_list), w.N, w.d)
+    Qd, Kd, Vd = oracle_operands(sel(q), sel(k), sel(v))
+    sub = Workload(w.name + "_heads", 1, len(bh_list), len(bh_list), w.N, w.d, causal=w.causal)
+    rows = sample_rows(sub, tiles_per_head=tiles_per_head).numpy()
+    Oo, Lo = oracle.fwd(Qd, Kd, Vd, causal=w.causal, rows=rows)
+    full = np.asarray(bh_list)[rows // w.N] * w.N + rows % w.N
+    assert_close(o.reshape(-1, w.d)[full], round_like(Oo, out_bf16), w.name + " O")
+    assert np.max(np.abs(lse.reshape(-1)[full] - Lo)) < 1e-3, w.name + " LSE"
+
+
 @pytest.mark.parametrize("w", [SWEEP[0], SWEEP[6 + 3]], ids=lambda w: w.name)
 def test_sweep_points_sampled(w):
     check(w, True, rows=sample_rows(w, tiles_per_head=3, heads=[0, w.B * w.Hq - 1]))
+
+
+@pytest.mark.parametrize("w", [SWEEP[2], SWEEP[3], SWEEP[4], SWEEP[5], SWEEP[11]], ids=lambda w: w.name)
+def test_sweep_long_points_sampled(w):
+    """d = 64 from N = 4096 up, and both N = 32768 points (256 key tiles: the
+    longest chains of running-max rescales), in the sweep's launch shape."""
+    check_heads(w, [0, w.B * w.Hq - 1], tiles_per_head=3)
 
 
 def test_train_causal_gqa_sampled():
