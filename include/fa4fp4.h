@@ -179,7 +179,7 @@ FA4FP4_API size_t fa4fp4_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int 
  * [B][Hkv][N][d], all f32, fully overwritten.  `workspace` must hold
  * fa4fp4_bwd_workspace_bytes(...) bytes (FA4FP4_ERR_WORKSPACE otherwise); it
  * receives the MXFP8 views of dO and D and must not be shared with another
- * call in flight.  Only d = 128 is supported (FA4FP4_ERR_UNSUPPORTED). */
+ * call in flight.  d = 64 or 128. */
 FA4FP4_API fa4fp4_status fa4fp4_bwd(const void* q4_codes, const void* q4_scales, const void* k4_codes,
                          const void* k4_scales, const void* q8c_codes, const void* q8c_scales,
                          const void* k8c_codes, const void* k8c_scales, const void* v8r_codes,

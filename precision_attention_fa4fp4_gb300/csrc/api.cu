@@ -274,7 +274,6 @@ fa4fp4_status fa4fp4_bwd(const void* q4c, const void* q4s, const void* k4c, cons
   if (o_dtype != FA4FP4_OUT_F32 && o_dtype != FA4FP4_OUT_BF16) return FA4FP4_ERR_INVALID_ARG;
   fa4fp4_status s = check_dims(B, Hq, Hkv, N, d);
   if (s != FA4FP4_OK) return s;
-  if (d != 128) return FA4FP4_ERR_UNSUPPORTED;
   if (B == 0 || Hq == 0) return FA4FP4_OK;
   const void* ptrs[] = {q4c, q4s, k4c, k4s, q8c, q8s, k8c, k8s, v8c, v8s, o, dout, lse, dq, dk, dv};
   for (const void* ptr : ptrs)
@@ -306,11 +305,15 @@ fa4fp4_status fa4fp4_bwd(const void* q4c, const void* q4s, const void* k4c, cons
   memset(&p, 0, sizeof(p));
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const uint64_t BHq = (uint64_t)B * Hq, BHk = (uint64_t)B * Hkv;
-  if (!make_map(&p.tm_k4, u8, 1, k4c, d / 2, N, BHk, d / 2, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&p.tm_v8r, u8, 1, v8c, d, N, BHk, d, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  // rows along d: d/2 bytes of E2M1 (64- or 32-byte swizzle), d bytes of E4M3
+  // (128- or 64-byte swizzle); rows along N: 128 or 64 bytes
+  const CUtensorMapSwizzle sw4 = d == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  const CUtensorMapSwizzle sw8 = d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  if (!make_map(&p.tm_k4, u8, 1, k4c, d / 2, N, BHk, d / 2, 128, sw4) ||
+      !make_map(&p.tm_v8r, u8, 1, v8c, d, N, BHk, d, 128, sw8) ||
       !make_map(&p.tm_k8c, u8, 1, k8c, Np, d, BHk, 128, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&p.tm_q4, u8, 1, q4c, d / 2, N, BHq, d / 2, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&p.tm_do_r, u8, 1, do_r, d, N, BHq, d, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&p.tm_q4, u8, 1, q4c, d / 2, N, BHq, d / 2, 64, sw4) ||
+      !make_map(&p.tm_do_r, u8, 1, do_r, d, N, BHq, d, 64, sw8) ||
       !make_map(&p.tm_q8c, u8, 1, q8c, Np, d, BHq, 64, d, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&p.tm_do_c, u8, 1, do_c, Np, d, BHq, 64, d, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&p.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq, d, N, BHq, d, 64, CU_TENSOR_MAP_SWIZZLE_NONE))

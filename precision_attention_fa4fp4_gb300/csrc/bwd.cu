@@ -27,6 +27,9 @@
 //                blocks of 32 keys (warp-wide max with redux.sync).
 //   warps 10-13  dQ^T from TMEM, times softmax_scale, added into dq.
 //   After the loop: dV and dK * softmax_scale written by warps 2-9.
+// d = 64 or 128 (template D).  Block-scaled MMAs have M = 128, so at d = 64
+// the A operand of dQ^T (K8c^T, d rows) is padded to 128 rows with zeros in
+// shared memory and the extra 64 TMEM lanes of dQ^T are not read.
 // The P/dS warps release S^T and dP^T as soon as they hold them in registers,
 // so S^T and dP^T of step t+1 run on the tensor core while step t's P and dS
 // are built; P, dS and their scale chunks are double-buffered by step parity.
@@ -41,7 +44,6 @@ constexpr int BK = 128;          // keys per CTA
 constexpr int BQ = 64;           // queries per step
 constexpr int NST = 3;           // input stages (Q4, dOr, Q8, dOc of a step)
 constexpr int BWD_GROUP = 4;     // causal CTA order: kv heads per group
-constexpr int D = 128;
 constexpr int NTHREADS = 14 * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_ST = 0, COL_DPT = 64, COL_DQT = 128, COL_DV = 192, COL_DK = 320,
@@ -49,13 +51,14 @@ constexpr uint32_t COL_ST = 0, COL_DPT = 64, COL_DQT = 128, COL_DV = 192, COL_DK
                    SF_Q4 = 472, SF_DOR = 480, SF_Q8 = 488, SF_DOC = 496;   // last four: [2 stages]
 static_assert(SF_DOC + 8 <= TMEM_COLS, "TMEM budget");
 
+template <int D>
 struct BL {   // shared-memory layout (bytes)
-  static constexpr int K4 = 0;                       // 128 keys x 64 B (E2M1, d=128)
-  static constexpr int V8 = K4 + BK * D / 2;         // 128 keys x 128 B (E4M3)
-  static constexpr int K8 = V8 + BK * D;             // 128 d-rows x 128 keys (E4M3)
-  static constexpr int STG = K8 + D * BK;            // stages
+  static constexpr int K4 = 0;                       // 128 keys x d/2 B (E2M1)
+  static constexpr int V8 = K4 + BK * D / 2;         // 128 keys x d B (E4M3)
+  static constexpr int K8 = V8 + BK * D;             // d rows x 128 keys (E4M3), zero rows up to 128
+  static constexpr int STG = K8 + 128 * BK;          // stages
   static constexpr int Q4 = 0, DOR = Q4 + BQ * D / 2, Q8 = DOR + BQ * D, DOC = Q8 + D * BQ;
-  static constexpr int STAGE_BYTES = DOC + D * BQ;   // 28 KB
+  static constexpr int STAGE_BYTES = DOC + D * BQ;   // 28 KB at d = 128, 14 KB at d = 64
   static constexpr int PQ = STG + NST * STAGE_BYTES; // [2] x 128 keys x 64 B
   static constexpr int DSC = PQ + 2 * BK * BQ;       // [2]
   static constexpr int DSR = DSC + 2 * BK * BQ;      // [2]
@@ -119,7 +122,14 @@ FA4_DEV void st_row_sw64(uint8_t* tile, int r, int g, uint4 lo, uint4 hi) {
   *reinterpret_cast<uint4*>(row + (((2 * g + 1) ^ x) << 4)) = hi;
 }
 
+template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
+  using BL = fa4::BL<D>;
+  // operand tiles with d-byte (E4M3) or d/2-byte (E2M1) rows along d
+  constexpr Swizzle SW4 = D == 128 ? SW_64B : SW_32B;     // Q4, K4
+  constexpr uint32_t SBO4 = D == 128 ? 512 : 256;
+  constexpr Swizzle SW8 = D == 128 ? SW_128B : SW_64B;    // V8r, dOr
+  constexpr uint32_t SBO8 = D == 128 ? 1024 : 512;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BL::BAR);
@@ -179,6 +189,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(tmem_holder, TMEM_COLS);
+  if (D < 128 && warp >= 2) {
+    // zero rows d..127 of the K8c^T operand (the TMA fills rows 0..d-1)
+    uint4* z = reinterpret_cast<uint4*>(smem + BL::K8 + D * BK);
+    for (int i = threadIdx.x - 64; i < (128 - D) * BK / 16; i += NTHREADS - 64) z[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -195,8 +211,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
       tma_load_3d(smem + BL::V8, &p.tm_v8r, fix_full, 0, k0, bkv);
       tma_load_3d(smem + BL::K8, &p.tm_k8c, fix_full, k0, 0, bkv);
     }
-    stage_chunk(sfc + 0 * 512, p.k4_s + ((long long)bkv * p.N + k0) * (D / 32), D / 32, nk_valid, 4, lane);
-    stage_chunk(sfc + 1 * 512, p.v8r_s + ((long long)bkv * p.N + k0) * (D / 32), D / 32, nk_valid, 4, lane);
+    stage_chunk(sfc + 0 * 512, p.k4_s + ((long long)bkv * p.N + k0) * (D / 32), D / 32, nk_valid, D / 32, lane);
+    stage_chunk(sfc + 1 * 512, p.v8r_s + ((long long)bkv * p.N + k0) * (D / 32), D / 32, nk_valid, D / 32, lane);
     stage_chunk(sfc + 2 * 512, p.k8c_s + (long long)bkv * D * (p.Np / 32) + k0 / 32, p.Np / 32, D, 4, lane);
     fence_proxy_async_smem();
     __syncwarp();
@@ -220,8 +236,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
       // scale chunks, LSE log2 e and D of the stage, while its tiles are in
       // flight: every load is issued before the first shared-memory store
       uint8_t* sc = sfc + (9 + 4 * st) * 512;
-      const uint4 c0 = load_chunk(p.q4_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, 4, lane);
-      const uint4 c1 = load_chunk(p.do_r_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, 4, lane);
+      const uint4 c0 = load_chunk(p.q4_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, D / 32, lane);
+      const uint4 c1 = load_chunk(p.do_r_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, D / 32, lane);
       const uint4 c2 = load_chunk(p.q8c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
       const uint4 c3 = load_chunk(p.do_c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
       float l2[2], dd[2];
@@ -257,7 +273,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
     const bool leader = elect_one();
     const uint32_t id_st = idesc_bs(128, BQ, 1, 1, false, false, 0, 0);      // mxf4
     const uint32_t id_dp = idesc_bs(128, BQ, 0, 0, false, false, 0, 0);      // mxf8 e4m3
-    const uint32_t id_acc = idesc_bs(128, D, 0, 0, false, false, 0, 0);
+    const uint32_t id_acc = idesc_bs(128, D, 0, 0, false, false, 0, 0);   // N = d
     const uint32_t id_dq = idesc_bs(128, BQ, 0, 0, false, true, 0, 0);
     const uint32_t s_k4 = smem_u32(smem + BL::K4), s_v8 = smem_u32(smem + BL::V8),
                    s_k8 = smem_u32(smem + BL::K8), s_pq = smem_u32(smem + BL::PQ),
@@ -285,17 +301,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
         tmem_cp_sf(tbase + SF_Q8 + 4 * sp, sc + 1024);
         tmem_cp_sf(tbase + SF_DOC + 4 * sp, sc + 1536);
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {     // K = d = 128: 2 x K64
+        for (int k = 0; k < D / 64; ++k) {     // K = d: K64 steps
           const uint32_t sf = ((uint32_t)(2 * k) << 29) | ((uint32_t)(2 * k) << 4);
-          mma_mxf4(tbase + COL_ST, make_sdesc(s_k4 + 32 * k, 16, 512, SW_64B),
-                   make_sdesc(sb + BL::Q4 + 32 * k, 16, 512, SW_64B), id_st | sf, tbase + SF_K4,
+          mma_mxf4(tbase + COL_ST, make_sdesc(s_k4 + 32 * k, 16, SBO4, SW4),
+                   make_sdesc(sb + BL::Q4 + 32 * k, 16, SBO4, SW4), id_st | sf, tbase + SF_K4,
                    tbase + SF_Q4 + 4 * sp, k > 0);
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {     // K = d: 4 x K32
+        for (int k = 0; k < D / 32; ++k) {     // K = d: K32 steps
           const uint32_t sf = ((uint32_t)k << 29) | ((uint32_t)k << 4);
-          mma_mxf8(tbase + COL_DPT, make_sdesc(s_v8 + 32 * k, 16, 1024, SW_128B),
-                   make_sdesc(sb + BL::DOR + 32 * k, 16, 1024, SW_128B), id_dp | sf, tbase + SF_V8,
+          mma_mxf8(tbase + COL_DPT, make_sdesc(s_v8 + 32 * k, 16, SBO8, SW8),
+                   make_sdesc(sb + BL::DOR + 32 * k, 16, SBO8, SW8), id_dp | sf, tbase + SF_V8,
                    tbase + SF_DOR + 4 * sp, k > 0);
         }
         mma_commit(s_full);
@@ -327,7 +343,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
                    make_sdesc(sb + BL::Q8 + 32 * k, 16, 512, SW_64B), id_acc | sf, tbase + SF_DSC,
                    tbase + SF_Q8 + 4 * sp, t > 0 || k > 0);
         }
-        // dQ^T = K8c^T dSr (K = 128 keys: 4 x K32; dSr stored [keys][64 q], MN-major)
+        // dQ^T = K8c^T dSr (K = 128 keys: 4 x K32; dSr stored [keys][64 q], MN-major;
+        // A has 128 rows: d rows of K8c^T, then zeros)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint32_t sf = ((uint32_t)k << 29) | ((uint32_t)k << 4);
@@ -468,7 +485,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
       const bool valid = key < p.N;
       const long long orow = ((long long)bkv * p.N + key) * D;
 #pragma unroll 1
-      for (int cc = 2 * g; cc < 2 * g + 2; ++cc) {    // 4 x 32 columns, 2 per group
+      for (int cc = (D / 64) * g; cc < (D / 64) * (g + 1); ++cc) {    // d/32 x 32 columns, half per group
         uint32_t v[32];
         tmem_ld32(lane_base + COL_DV + 32 * cc, v);
         tmem_ld_wait();
@@ -524,10 +541,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
       if (lane == 0) okw[warp - 10] = all_ok ? 1 : 0;
       named_bar(1, 128);
       if (!(okw[0] & okw[1] & okw[2] & okw[3])) break;
+      if (drow < D) {     // TMEM lanes d..127 hold the zero rows of the padded operand
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        stage[i * D + drow] = __uint_as_float(v0[i]) * p.scale;
-        stage[(32 + i) * D + drow] = __uint_as_float(v1[i]) * p.scale;
+        for (int i = 0; i < 32; ++i) {
+          stage[i * D + drow] = __uint_as_float(v0[i]) * p.scale;
+          stage[(32 + i) * D + drow] = __uint_as_float(v1[i]) * p.scale;
+        }
       }
       fence_proxy_async_smem();
       named_bar(1, 128);
@@ -544,32 +563,61 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
 }
 
 // D_i = sum_t dO_it * O_it (one warp per row) and dq = 0.
-template <bool O_BF16>
+template <int D, bool O_BF16>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const void* __restrict__ o,
                                                         const __nv_bfloat16* __restrict__ dout,
                                                         long long rows, float* __restrict__ Dvec,
                                                         float* __restrict__ dq) {
   const int lane = threadIdx.x % 32;
   const long long wpb = blockDim.x / 32;
+  constexpr int E = D / 32;     // elements per lane: 4 (d = 128) or 2 (d = 64)
   for (long long row = blockIdx.x * wpb + threadIdx.x / 32; row < rows; row += (long long)gridDim.x * wpb) {
-    const long long base = row * D + lane * 4;
-    const uint2 dw = *reinterpret_cast<const uint2*>(dout + base);
-    float dof[4] = {__uint_as_float(dw.x << 16), __uint_as_float(dw.x & 0xffff0000u),
-                    __uint_as_float(dw.y << 16), __uint_as_float(dw.y & 0xffff0000u)};
-    float of[4];
-    if (O_BF16) {
-      const uint2 ow = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(o) + base);
-      of[0] = __uint_as_float(ow.x << 16); of[1] = __uint_as_float(ow.x & 0xffff0000u);
-      of[2] = __uint_as_float(ow.y << 16); of[3] = __uint_as_float(ow.y & 0xffff0000u);
+    const long long base = row * D + lane * E;
+    uint32_t dw[E / 2];
+    float dof[E], of[E];
+    if constexpr (E == 4) {
+      const uint2 t = *reinterpret_cast<const uint2*>(dout + base);
+      dw[0] = t.x; dw[1] = t.y;
     } else {
-      const float4 ov = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(o) + base);
-      of[0] = ov.x; of[1] = ov.y; of[2] = ov.z; of[3] = ov.w;
+      dw[0] = *reinterpret_cast<const uint32_t*>(dout + base);
     }
-    float acc = dof[0] * of[0] + dof[1] * of[1] + dof[2] * of[2] + dof[3] * of[3];
+#pragma unroll
+    for (int u = 0; u < E / 2; ++u) {
+      dof[2 * u] = __uint_as_float(dw[u] << 16);
+      dof[2 * u + 1] = __uint_as_float(dw[u] & 0xffff0000u);
+    }
+    if constexpr (O_BF16) {
+      uint32_t ow[E / 2];
+      const __nv_bfloat16* ob = reinterpret_cast<const __nv_bfloat16*>(o) + base;
+      if constexpr (E == 4) {
+        const uint2 t = *reinterpret_cast<const uint2*>(ob);
+        ow[0] = t.x; ow[1] = t.y;
+      } else {
+        ow[0] = *reinterpret_cast<const uint32_t*>(ob);
+      }
+#pragma unroll
+      for (int u = 0; u < E / 2; ++u) {
+        of[2 * u] = __uint_as_float(ow[u] << 16);
+        of[2 * u + 1] = __uint_as_float(ow[u] & 0xffff0000u);
+      }
+    } else {
+      const float* of32 = reinterpret_cast<const float*>(o) + base;
+      if constexpr (E == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(of32);
+        of[0] = t.x; of[1] = t.y; of[2] = t.z; of[3] = t.w;
+      } else {
+        const float2 t = *reinterpret_cast<const float2*>(of32);
+        of[0] = t.x; of[1] = t.y;
+      }
+    }
+    float acc = 0.f;
+#pragma unroll
+    for (int u = 0; u < E; ++u) acc += dof[u] * of[u];
 #pragma unroll
     for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) Dvec[row] = acc;
-    *reinterpret_cast<float4*>(dq + base) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (E == 4) *reinterpret_cast<float4*>(dq + base) = make_float4(0.f, 0.f, 0.f, 0.f);
+    else *reinterpret_cast<float2*>(dq + base) = make_float2(0.f, 0.f);
   }
 }
 
@@ -582,18 +630,28 @@ cudaError_t launch_bwd_prep(const BwdPrepParams& p, cudaStream_t st) {
   if ((e = launch_quantize(p.dout, rows, p.d, p.N, (long long)p.B * p.Hq, 1, 1, p.do_c, p.do_c_s, st)) != cudaSuccess) return e;
   long long blocks = (rows + 7) / 8;
   int grid = (int)(blocks < 152 * 16 ? blocks : 152 * 16);
-  if (p.o_bf16)
-    bwd_prep_kernel<true><<<grid, 256, 0, st>>>(p.o, (const __nv_bfloat16*)p.dout, rows, p.Dvec, p.dq);
-  else
-    bwd_prep_kernel<false><<<grid, 256, 0, st>>>(p.o, (const __nv_bfloat16*)p.dout, rows, p.Dvec, p.dq);
+  const __nv_bfloat16* dout = (const __nv_bfloat16*)p.dout;
+  if (p.d == 128) {
+    if (p.o_bf16) bwd_prep_kernel<128, true><<<grid, 256, 0, st>>>(p.o, dout, rows, p.Dvec, p.dq);
+    else bwd_prep_kernel<128, false><<<grid, 256, 0, st>>>(p.o, dout, rows, p.Dvec, p.dq);
+  } else {
+    if (p.o_bf16) bwd_prep_kernel<64, true><<<grid, 256, 0, st>>>(p.o, dout, rows, p.Dvec, p.dq);
+    else bwd_prep_kernel<64, false><<<grid, 256, 0, st>>>(p.o, dout, rows, p.Dvec, p.dq);
+  }
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_bwd_main_t(const BwdParams& p, cudaStream_t st) {
+  const dim3 grid((unsigned)((p.N + BK - 1) / BK) * (unsigned)(p.B * p.Hkv));
+  auto k = bwd_kernel<D>;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, BL<D>::BYTES);
+  k<<<grid, NTHREADS, BL<D>::BYTES, st>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t st) {
-  const dim3 grid((unsigned)((p.N + BK - 1) / BK) * (unsigned)(p.B * p.Hkv));
-  cudaFuncSetAttribute(bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BL::BYTES);
-  bwd_kernel<<<grid, NTHREADS, BL::BYTES, st>>>(p);
-  return cudaGetLastError();
+  return p.d == 128 ? launch_bwd_main_t<128>(p, st) : launch_bwd_main_t<64>(p, st);
 }
 
 }  // namespace fa4

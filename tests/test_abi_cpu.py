@@ -121,8 +121,10 @@ def test_empty_problems_are_noops(lib):
     assert lib.fa4fp4_fwd(*n6, 0, 4, 3, 64, 64, 0.0, 0, null, 1, null, null) == UNSUP
     assert lib.fa4fp4_fwd(*n6, 0, 4, 4, 64, 64, 0.0, 0, null, 9, null, null) == INVALID
     assert lib.fa4fp4_fwd_nvfp4(*([null] * 8), 0, 4, 4, 64, 64, 0.0, 0, 5, null, 1, null, null) == INVALID
-    assert lib.fa4fp4_bwd(*([null] * 11), 0, null, null, 0, 4, 2, 300, 64, 0.0, 1,
+    assert lib.fa4fp4_bwd(*([null] * 11), 0, null, null, 0, 4, 2, 300, 96, 0.0, 1,
                           null, null, null, null, 0, null) == UNSUP
+    assert lib.fa4fp4_bwd(*([null] * 11), 0, null, null, 0, 4, 2, 300, 64, 0.0, 1,
+                          null, null, null, null, 0, null) == OK
     assert lib.fa4fp4_quantize_qkv(null, null, null, -1, 4, 2, 64, 128, *n6, null) == INVALID
 
 

@@ -73,6 +73,19 @@ def test_small(N, causal):
     check(Workload(f"bwd_n{N}", 1, 4, 2, N, 128, causal=causal, qk_std=128 ** -0.25), seed=N)
 
 
+@pytest.mark.parametrize("N", [1, 64, 129, 300, 1000])
+@pytest.mark.parametrize("causal", [True, False])
+def test_d64(N, causal):
+    """Head dimension 64: GQA groups of two, ragged N (one key, partial key
+    tiles, partial 64-query steps)."""
+    check(Workload(f"bwd_d64_n{N}", 1, 4, 2, N, 64, causal=causal, qk_std=64 ** -0.25), seed=N + 64)
+
+
+def test_d64_mqa_two_batches_bf16_o():
+    check(Workload("bwd_d64_b2_mqa_n257", 2, 4, 1, 257, 64, causal=True, qk_std=64 ** -0.25), seed=5,
+          o_bf16=True)
+
+
 def test_train_causal_gqa_sampled():
     """Causal GQA training shape: the kv head (b=1, hk=5) in full for dK/dV on
     its first and last key tiles, dQ on two query tiles of its first head."""
