@@ -15,10 +15,10 @@
 //               loaded once for both query tiles.
 //   warp 1      TMEM allocation; one elected lane issues tcgen05.cp (scale
 //               factors) and tcgen05.mma kind::mxf4 block_scale: S = Q_X K_j^T
-//               into one S buffer that the two query tiles take in turn,
-//               O_X += P_X V_j, and l_X += P_X 1 (an N=16 MMA against an
-//               all-ones E2M1 tile, so the normalizer is summed by the tensor
-//               core from exactly the codes P V consumes).
+//               into one S buffer that the two query tiles take in turn, and
+//               [O_X | l_X] += P_X [V_j | 1]: the V^T operand carries 16 extra
+//               rows of E2M1 ones under unit scales, so the same MMA (N = d +
+//               16) sums the normalizer from exactly the codes P V consumes.
 //   warps 2-5   softmax of tile A, warps 6-9 softmax of tile B: one thread per
 //               query row (TMEM lane quadrant = warp mod 4), holding the row's
 //               128 scores of the key tile.  Row max, Direct-P codes (native
@@ -39,7 +39,7 @@ constexpr int BN = 128;         // keys per tile
 constexpr int NSOFT = 8;        // softmax warps: 4 per query tile
 constexpr int NTHREADS = 32 * (2 + NSOFT);
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S = 0, COL_O0 = 128, COL_L0 = 384;   // O_X at 128 + 128X, l_X at 384 + 16X
+constexpr uint32_t COL_S = 0, COL_O0 = 128;   // [O_X | l_X] at 128 + (d + 16) X
 
 // Shared-memory and TMEM layout of one CTA.  P8: the FP8 P/V route (E4M3 P
 // and V^T, one E8M0 scale per 32 keys), else Direct-P (E2M1 P and V^T).
@@ -49,21 +49,21 @@ template <int D, bool P8, bool NV>
 struct Layout {
   static constexpr int QSB = NV ? D / 16 : D / 32;   // scale bytes per Q/K row
   static constexpr int NSC = NV ? D / 64 : 1;        // scale chunks per Q/K tile
-  static constexpr int STAGES = P8 ? 4 : 6;   // K/V pipeline depth
+  static constexpr int STAGES = P8 ? 4 : ((NV && D == 128) ? 4 : 6);   // K/V pipeline depth
+  static constexpr int NO = D + 16;           // columns of [O_X | l_X]: d of O, 16 copies of l
   static constexpr int QB = BM * D / 2;       // bytes of a Q or K code tile
   static constexpr int KB = BN * D / 2;
   static constexpr int PROW = P8 ? BN : BN / 2;   // bytes of a P (or V^T) row of 128 keys
-  static constexpr int VB = D * PROW;         // V^T: D rows of 128 keys
+  static constexpr int VD = D * PROW;         // V^T: d channel rows of 128 keys (the TMA box)
+  static constexpr int VB = NO * PROW;        // a V stage: the d rows, then 16 rows of ones
   static constexpr int PB = BM * PROW;
-  static constexpr int ONESB = 16 * PROW;     // 16 rows of 128 ones
   static constexpr int OFF_Q = 0;                          // Q_A, Q_B
   static constexpr int OFF_K = OFF_Q + 2 * QB;
   static constexpr int OFF_V = OFF_K + STAGES * KB;
   static constexpr int OFF_P = OFF_V + STAGES * VB;        // [tile X][2 buffers]
-  static constexpr int OFF_ONES = OFF_P + 4 * PB;
-  static constexpr int OFF_SF = OFF_ONES + ONESB;         // 512-byte scale chunks
+  static constexpr int OFF_SF = OFF_P + 4 * PB;           // 512-byte scale chunks
   static constexpr int SF_Q = OFF_SF;                     // [X][NSC]
-  static constexpr int SF_1 = SF_Q + 2 * NSC * 512;       // unit scales (ones tile; Direct-P P)
+  static constexpr int SF_1 = SF_Q + 2 * NSC * 512;       // unit scales (ones rows of V^T; Direct-P P)
   static constexpr int SF_P = SF_1 + 512;                 // P8: [X][step parity]
   static constexpr int SF_K = SF_P + (P8 ? 4 * 512 : 0);  // [stage][NSC]
   static constexpr int SF_V = SF_K + 512 * NSC * STAGES;
@@ -72,9 +72,16 @@ struct Layout {
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int BYTES = OFF_MISC + 64 + 1024;    // + alignment slack
   // TMEM scale-factor columns (4 per chunk): Q_X, unit, P_X (P8), K and V rings
+  // TMEM scale-factor columns (4 per chunk): Q_X, unit, P_X (P8), K and V
+  // rings.  A V stage's scales cover its d + 16 rows (row r in column r/32):
+  // at d = 64 the ones rows 64..79 fall in the chunk's third column, at
+  // d = 128 rows 128..143 need a fifth column, so the stage takes 8 columns,
+  // the upper four holding unit scales.
+  static constexpr uint32_t SFVS = D == 128 ? 8 : 4;
   static constexpr uint32_t COL_SFQ0 = 416, COL_SF1 = COL_SFQ0 + 8 * NSC, COL_SFP0 = COL_SF1 + 4,
                             COL_SFK = COL_SFP0 + (P8 ? 8 : 0), COL_SFV = COL_SFK + 4 * NSC * STAGES;
-  static_assert(COL_SFV + 4 * STAGES <= TMEM_COLS, "TMEM budget");
+  static_assert(COL_O0 + 2 * NO <= COL_SFQ0, "TMEM budget: S, O_A, O_B");
+  static_assert(COL_SFV + SFVS * STAGES <= TMEM_COLS, "TMEM budget");
   static_assert(BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -217,14 +224,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
     fence_barrier_init();
   }
   if (warp == 1) {
-    // unit E8M0 scale (byte 127) for the ones tile (and every Direct-P P
-    // block); the ones tile holds 1.0 in every element: E2M1 code 2 per nibble
-    // or E4M3 code 0x38 per byte
+    // unit E8M0 scales (byte 127) for the ones rows (and every Direct-P P
+    // block); the 16 ones rows after the d channel rows of every V stage hold
+    // 1.0 in every element: E2M1 code 2 per nibble or E4M3 code 0x38 per byte
     reinterpret_cast<uint4*>(smem + L::SF_1)[lane] = make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
     const uint32_t one = P8 ? 0x38383838u : 0x22222222u;
-#pragma unroll
-    for (int i = 0; i < L::ONESB / 512; ++i)
-      reinterpret_cast<uint4*>(smem + L::OFF_ONES)[lane + 32 * i] = make_uint4(one, one, one, one);
+    for (int st = 0; st < STAGES; ++st)
+      for (int i = lane; i < L::PROW; i += 32)    // 16 rows x PROW bytes = PROW 16-byte words
+        reinterpret_cast<uint4*>(smem + L::OFF_V + st * L::VB + L::VD)[i] = make_uint4(one, one, one, one);
+    if constexpr (D == 64) {
+      // V scale chunks: rows 64..79 (column 2, lanes 0..15) unit, rows 80..127
+      // zero; the producer refreshes rows 0..63 for every key tile
+      for (int st = 0; st < STAGES; ++st) {
+        uint32_t* w = reinterpret_cast<uint32_t*>(smem + L::SF_V + 512 * st) + lane * 4;
+        w[2] = lane < 16 ? 0x7f7f7f7fu : 0u;
+        w[3] = 0u;
+      }
+    }
     fence_proxy_async_smem();
     tmem_alloc(tmem_holder, TMEM_COLS);
   }
@@ -306,15 +322,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       if (j >= STAGES && !mbar_wait(&v_empty[st], ph, abort_flag, p.err)) break;
       uint8_t* vchunk = smem + L::SF_V + 512 * st;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int ch = lane + 32 * c;
-        const bool in = ch < D;
-        cp_async4(vchunk + lane * 16 + 4 * c, vs + (long long)(in ? ch : 0) * (p.Np / 32) + 4 * j, in ? 4u : 0u);
-      }
+      for (int c = 0; c < D / 32; ++c)   // the d channel rows (the ones rows' scales are fixed)
+        cp_async4(vchunk + lane * 16 + 4 * c, vs + (long long)(lane + 32 * c) * (p.Np / 32) + 4 * j, 4u);
       cp_async_mbar_arrive(&v_full[st]);
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(&v_full[st], L::VB);
+        mbar_arrive_expect_tx(&v_full[st], L::VD);
         tma_load_3d(smem + L::OFF_V + st * L::VB, &p.tm_v, &v_full[st], j * L::PROW, 0, bkv);
       }
       issued = j + 1;
@@ -334,13 +347,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
     const bool leader = elect_one();
     constexpr int KSTEPS = D / 64;   // K = 64 per mxf4 MMA
     const uint32_t idesc_s = idesc_bs(BM, BN, 1, 1, false, false, 0, 0);
-    // P V and the normalizer: E2M1 (kind::mxf4 code 1) or E4M3 (kind::mxf8f6f4 code 0)
-    const uint32_t idesc_o = idesc_bs(BM, D, P8 ? 0 : 1, P8 ? 0 : 1, false, false, 0, 0);
-    const uint32_t idesc_l = idesc_bs(BM, 16, P8 ? 0 : 1, P8 ? 0 : 1, false, false, 0, 0);
+    // [O | l] += P [V | 1]: E2M1 (kind::mxf4 code 1) or E4M3 (kind::mxf8f6f4 code 0), N = d + 16
+    const uint32_t idesc_o = idesc_bs(BM, L::NO, P8 ? 0 : 1, P8 ? 0 : 1, false, false, 0, 0);
     constexpr Swizzle QSW = D == 128 ? SW_64B : SW_32B;
     constexpr uint32_t QSBO = D == 128 ? 512 : 256;
     const uint32_t sq = smem_u32(smem + L::OFF_Q);
-    const uint32_t sones = smem_u32(smem + L::OFF_ONES);
     bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
     fence_proxy_async_smem();   // Q scale words written by cp.async
     tc_fence_after();
@@ -348,6 +359,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
 #pragma unroll
       for (int i = 0; i < 2 * NSC; ++i) tmem_cp_sf(tbase + COL_SFQ0 + 4 * i, smem + L::SF_Q + 512 * i);
       tmem_cp_sf(tbase + COL_SF1, smem + L::SF_1);
+      if constexpr (D == 128) {
+        // unit scales of the ones rows 128..143 of every V stage (fifth column)
+#pragma unroll
+        for (int st = 0; st < STAGES; ++st) tmem_cp_sf(tbase + COL_SFV + L::SFVS * st + 4, smem + L::SF_1);
+      }
     }
     __syncwarp();
     // S = Q_X K_t^T once the other tile's warps hold their S (first = no wait)
@@ -390,13 +406,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       __syncwarp();
       return true;
     };
-    // O_X += P_X V_t, l_X += P_X 1
+    // [O_X | l_X] += P_X [V_t | 1]
     auto issue_pv = [&](int x, int t) -> bool {
       const int st = t % STAGES;
       if (x == 0) {
         if (!mbar_wait(&v_full[st], (t / STAGES) & 1, abort_flag, p.err)) return false;
         fence_proxy_async_smem();
-        if (leader) tmem_cp_sf(tbase + COL_SFV + 4 * st, smem + L::SF_V + 512 * st);
+        if (leader) tmem_cp_sf(tbase + COL_SFV + L::SFVS * st, smem + L::SF_V + 512 * st);
         __syncwarp();
       }
       if (!mbar_wait(&p_full[x], t & 1, abort_flag, p.err)) return false;
@@ -411,20 +427,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
           for (int k = 0; k < 4; ++k) {   // 128 keys = 4 x K32
             const uint64_t ad = make_sdesc(sp + 32 * k, 16, 1024, SW_128B);
             const uint32_t sf = ((uint32_t)k << 29) | ((uint32_t)k << 4);
-            mma_mxf8(tbase + COL_O0 + 128 * x, ad, make_sdesc(sv + 32 * k, 16, 1024, SW_128B), idesc_o | sf,
-                     tbase + COL_SFP0 + 4 * x, tbase + COL_SFV + 4 * st, t > 0 || k > 0);
-            mma_mxf8(tbase + COL_L0 + 16 * x, ad, make_sdesc(sones + 32 * k, 16, 1024, SW_128B), idesc_l | sf,
-                     tbase + COL_SFP0 + 4 * x, tbase + COL_SF1, t > 0 || k > 0);
+            mma_mxf8(tbase + COL_O0 + L::NO * x, ad, make_sdesc(sv + 32 * k, 16, 1024, SW_128B), idesc_o | sf,
+                     tbase + COL_SFP0 + 4 * x, tbase + COL_SFV + L::SFVS * st, t > 0 || k > 0);
           }
         } else {
 #pragma unroll
           for (int k = 0; k < 2; ++k) {   // 128 keys = 2 x K64
             const uint64_t ad = make_sdesc(sp + 32 * k, 16, 512, SW_64B);
             const uint32_t sf = ((uint32_t)(2 * k) << 29) | ((uint32_t)(2 * k) << 4);
-            mma_mxf4(tbase + COL_O0 + 128 * x, ad, make_sdesc(sv + 32 * k, 16, 512, SW_64B), idesc_o | sf,
-                     tbase + COL_SF1, tbase + COL_SFV + 4 * st, t > 0 || k > 0);
-            mma_mxf4(tbase + COL_L0 + 16 * x, ad, make_sdesc(sones + 32 * k, 16, 512, SW_64B), idesc_l | sf,
-                     tbase + COL_SF1, tbase + COL_SF1, t > 0 || k > 0);
+            mma_mxf4(tbase + COL_O0 + L::NO * x, ad, make_sdesc(sv + 32 * k, 16, 512, SW_64B), idesc_o | sf,
+                     tbase + COL_SF1, tbase + COL_SFV + L::SFVS * st, t > 0 || k > 0);
           }
         }
         mma_commit(&o_done[x]);
@@ -548,8 +560,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
           // the row of O_X and l_X in one TMEM round trip
           uint32_t ov[D / 32][32];
 #pragma unroll
-          for (int g = 0; g < D / 32; ++g) tmem_ld32(lane_base + COL_O0 + 128 * x + 32 * g, ov[g]);
-          uint32_t lv = tmem_ld1(lane_base + COL_L0 + 16 * x);
+          for (int g = 0; g < D / 32; ++g) tmem_ld32(lane_base + COL_O0 + L::NO * x + 32 * g, ov[g]);
+          uint32_t lv = tmem_ld1(lane_base + COL_O0 + L::NO * x + D);
           tmem_ld_wait_regs(ov[0], lv);
 #pragma unroll
           for (int g = 0; g < D / 32; ++g) {
@@ -561,9 +573,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
               ov[g][i] = __float_as_uint(t.x);
               ov[g][i + 1] = __float_as_uint(t.y);
             }
-            tmem_st32(lane_base + COL_O0 + 128 * x + 32 * g, ov[g]);
+            tmem_st32(lane_base + COL_O0 + L::NO * x + 32 * g, ov[g]);
           }
-          tmem_st1(lane_base + COL_L0 + 16 * x, __float_as_uint(__uint_as_float(lv) * alpha));
+          tmem_st1(lane_base + COL_O0 + L::NO * x + D, __float_as_uint(__uint_as_float(lv) * alpha));
           tmem_st_wait();
         }
       }
@@ -574,7 +586,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
     }
     if (ok && nt > 0 && mbar_wait(&o_done[x], (nt - 1) & 1, abort_flag, p.err)) {
       tc_fence_after();
-      const float l = __uint_as_float(tmem_ld1(lane_base + COL_L0 + 16 * x));
+      const float l = __uint_as_float(tmem_ld1(lane_base + COL_O0 + L::NO * x + D));
       tmem_ld_wait();
       const float inv_l = 1.f / l;
       const bool valid = qi < p.N;
@@ -582,7 +594,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
 #pragma unroll
       for (int g = 0; g < D / 32; ++g) {
         uint32_t v[32];
-        tmem_ld32(lane_base + COL_O0 + 128 * x + 32 * g, v);
+        tmem_ld32(lane_base + COL_O0 + L::NO * x + 32 * g, v);
         tmem_ld_wait();
         reg_fence32(v);
         if (valid && p.out_bf16) {
