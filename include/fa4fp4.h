@@ -158,6 +158,27 @@ FA4FP4_API fa4fp4_status fa4fp4_fwd_nvfp4(const void* q_codes, const void* q_sca
                                           int N, int d, float softmax_scale, int causal, int fp8pv, void* o,
                                           int out_dtype, float* lse, void* stream);
 
+/* Direct-P forward (or the FP8 P/V route, fp8pv = 1) with Q in bf16: Q is
+ * quantized to MXFP4 (E8M0 per 32 along d, the fa4fp4_quantize rule) inside
+ * the forward's prologue, so an inference step reads Q once and needs no
+ * separate pass over it (technical summary, Methodology 2 "Gradient Formats":
+ * quantization happens where the operands are produced, not as a pass of its
+ * own).  q: bf16 [B][Hq][N][d]; k, vt as in fa4fp4_fwd (vt MXFP8 along N when
+ * fp8pv = 1).  Results are identical, bit for bit, to fa4fp4_quantize of Q
+ * followed by fa4fp4_fwd (fa4fp4_fwd_fp8pv).  Errors as fa4fp4_fwd. */
+FA4FP4_API fa4fp4_status fa4fp4_fwd_qbf16(const void* q, const void* k_codes, const void* k_scales,
+                               const void* vt_codes, const void* vt_scales, int B, int Hq, int Hkv,
+                               int N, int d, float softmax_scale, int causal, int fp8pv, void* o,
+                               int out_dtype, float* lse, void* stream);
+
+/* K (MXFP4 along d) and V (MXFP4 along N, transposed) in one launch: the
+ * operands fa4fp4_fwd_qbf16 takes quantized.  Byte-identical to two
+ * fa4fp4_quantize calls.  k, v: bf16 [B][Hkv][N][d]; outputs in the layouts
+ * of fa4fp4_qtensor_bytes. */
+FA4FP4_API fa4fp4_status fa4fp4_quantize_kv(const void* k, const void* v, int B, int Hkv, int N, int d,
+                                 void* k_codes, void* k_scales, void* vt_codes, void* vt_scales,
+                                 void* stream);
+
 /* Bytes of caller-provided workspace fa4fp4_bwd needs. */
 FA4FP4_API size_t fa4fp4_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
 

@@ -60,6 +60,10 @@ def load_library():
         lib.fa4fp4_fwd_nvfp4.argtypes = [vp] * 8 + [i, i, i, i, i, f, i, i, vp, i, vp, vp]
         lib.fa4fp4_fwd.restype = i
         lib.fa4fp4_fwd.argtypes = [vp] * 6 + [i, i, i, i, i, f, i, vp, i, vp, vp]
+        lib.fa4fp4_fwd_qbf16.restype = i
+        lib.fa4fp4_fwd_qbf16.argtypes = [vp] * 5 + [i, i, i, i, i, f, i, i, vp, i, vp, vp]
+        lib.fa4fp4_quantize_kv.restype = i
+        lib.fa4fp4_quantize_kv.argtypes = [vp, vp, i, i, i, i, vp, vp, vp, vp, vp]
         lib.fa4fp4_bwd_workspace_bytes.restype = sz
         lib.fa4fp4_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
         lib.fa4fp4_bwd.restype = i
@@ -221,6 +225,59 @@ def fwd(q: QTensor, k: QTensor, vt: QTensor, causal: bool = False, softmax_scale
         _ptr(q.codes), _ptr(q.scales), _ptr(k.codes), _ptr(k.scales), _ptr(vt.codes), _ptr(vt.scales),
         B, Hq, Hkv, N, d, float(softmax_scale), int(bool(causal)), _ptr(out), out_dtype,
         _ptr(lse) if with_lse else None, _stream(dev)))
+    return out, (lse if with_lse else None)
+
+
+def quantize_kv(k: torch.Tensor, v: torch.Tensor, out=None):
+    """K (MXFP4 along d) and V (MXFP4 along N) in one launch
+    (fa4fp4_quantize_kv).  Returns (k4, vt) as quantize would."""
+    for t in (k, v):
+        if t.dtype != torch.bfloat16 or t.dim() != 4:
+            raise ValueError("quantize_kv expects bf16 [B,H,N,d] tensors")
+    if v.shape != k.shape:
+        raise ValueError("quantize_kv: k and v must have the same shape")
+    B, Hkv, N, d = k.shape
+    if out is not None:
+        _expect_qt("out[0] (k)", out[0], FMT_MXFP4, ALONG_D, (B, Hkv, N, d))
+        _expect_qt("out[1] (v)", out[1], FMT_MXFP4, ALONG_N, (B, Hkv, N, d))
+        _cuda(*_qt_buffers(*out))
+    _cuda(k, v)
+    if out is None:
+        out = (qtensor_alloc(B, Hkv, N, d, FMT_MXFP4, ALONG_D, k.device),
+               qtensor_alloc(B, Hkv, N, d, FMT_MXFP4, ALONG_N, k.device))
+    k4, vt = out
+    _check("fa4fp4_quantize_kv", load_library().fa4fp4_quantize_kv(
+        _ptr(k), _ptr(v), B, Hkv, N, d, _ptr(k4.codes), _ptr(k4.scales), _ptr(vt.codes), _ptr(vt.scales),
+        _stream(k.device)))
+    return k4, vt
+
+
+def fwd_qbf16(q: torch.Tensor, k: QTensor, vt: QTensor, causal: bool = False, softmax_scale: float = 0.0,
+              out_dtype: int = OUT_BF16, with_lse: bool = True, out=None, lse=None):
+    """Forward with bf16 Q quantized to MXFP4 in the kernel's prologue
+    (fa4fp4_fwd_qbf16).  vt MXFP4 along N gives Direct-P, MXFP8 along N the
+    FP8 P/V route.  Returns (o, lse or None), identical to quantize(q)
+    followed by fwd (fwd_fp8pv)."""
+    if q.dtype != torch.bfloat16 or q.dim() != 4:
+        raise ValueError("fwd_qbf16 expects a bf16 [B,H,N,d] q")
+    if not isinstance(vt, QTensor) or vt.fmt not in (FMT_MXFP4, FMT_MXFP8):
+        raise ValueError("vt: expected an MXFP4 or MXFP8 QTensor blocked along N")
+    fp8pv = 1 if vt.fmt == FMT_MXFP8 else 0
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    _expect_qt("k", k, FMT_MXFP4, ALONG_D, (B, Hkv, N, d))
+    _expect_qt("vt", vt, vt.fmt, ALONG_N, (B, Hkv, N, d))
+    _expect_out(out, lse if with_lse else None, B, Hq, N, d, out_dtype)
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, Hq, N, d), dtype=torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32, device=dev)
+    if with_lse and lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    _cuda(q, k.codes, k.scales, vt.codes, vt.scales, out, lse)
+    _check("fa4fp4_fwd_qbf16", load_library().fa4fp4_fwd_qbf16(
+        _ptr(q), _ptr(k.codes), _ptr(k.scales), _ptr(vt.codes), _ptr(vt.scales), B, Hq, Hkv, N, d,
+        float(softmax_scale), int(bool(causal)), fp8pv, _ptr(out), out_dtype, _ptr(lse) if with_lse else None,
+        _stream(dev)))
     return out, (lse if with_lse else None)
 
 

@@ -160,14 +160,20 @@ fa4fp4_status fa4fp4_quantize_qkv(const void* q, const void* k, const void* v, i
 
 // Shared by the Direct-P forward (fp8pv = 0, V^T MXFP4) and the FP8 P/V
 // route (fp8pv = 1, V^T MXFP8).
+// q_bf16 non-null: Q is bf16 [B][Hq][N][d], quantized to MXFP4 by the
+// kernel's prologue (qc, qs unused).
 static fa4fp4_status fwd_common(const void* qc, const void* qs, const void* kc, const void* ks,
                                 const void* vc, const void* vs, int B, int Hq, int Hkv, int N, int d,
                                 float softmax_scale, int causal, void* o, int out_dtype, float* lse,
-                                int fp8pv, const float* ts_q, const float* ts_k, void* stream) {
+                                int fp8pv, const float* ts_q, const float* ts_k, void* stream,
+                                const void* q_bf16 = nullptr) {
   if (out_dtype != FA4FP4_OUT_F32 && out_dtype != FA4FP4_OUT_BF16) return FA4FP4_ERR_INVALID_ARG;
   fa4fp4_status s = check_dims(B, Hq, Hkv, N, d);
   if (s != FA4FP4_OK) return s;
   if (B == 0 || Hq == 0) return FA4FP4_OK;
+  if (q_bf16) {
+    qc = qs = q_bf16;     // validated below like the code and scale pointers
+  }
   if (!qc || !qs || !kc || !ks || !vc || !vs || !o) return FA4FP4_ERR_INVALID_ARG;
   if ((ts_q == nullptr) != (ts_k == nullptr)) return FA4FP4_ERR_INVALID_ARG;
   if ((ts_q && (reinterpret_cast<uintptr_t>(ts_q) & 3)) || (ts_k && (reinterpret_cast<uintptr_t>(ts_k) & 3)))
@@ -183,7 +189,7 @@ static fa4fp4_status fwd_common(const void* qc, const void* qs, const void* kc, 
   // V^T rows of 128 keys: 64 bytes of E2M1 (64-byte swizzle) or 128 bytes of
   // E4M3 (128-byte swizzle)
   const int vrow = fp8pv ? 128 : 64;
-  if (!make_map(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qc, d / 2, N, (uint64_t)B * Hq, d / 2, 128, qsw) ||
+  if ((!q_bf16 && !make_map(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qc, d / 2, N, (uint64_t)B * Hq, d / 2, 128, qsw)) ||
       !make_map(&p.tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kc, d / 2, N, (uint64_t)B * Hkv, d / 2, 128, qsw) ||
       !make_map(&p.tm_v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, vc, fp8pv ? Np : Np / 2, d, (uint64_t)B * Hkv, vrow, d,
                 fp8pv ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
@@ -201,6 +207,7 @@ static fa4fp4_status fwd_common(const void* qc, const void* qs, const void* kc, 
   p.fp8pv = fp8pv;
   p.ts_q = ts_q;
   p.ts_k = ts_k;
+  p.q_bf16 = q_bf16;
   p.scale = default_scale(softmax_scale, d);
   p.c = (float)((double)p.scale * 1.4426950408889634);
   const float* T = directp_thresholds();
@@ -222,6 +229,30 @@ fa4fp4_status fa4fp4_fwd_fp8pv(const void* qc, const void* qs, const void* kc, c
                                void* stream) {
   return fwd_common(qc, qs, kc, ks, v8c, v8s, B, Hq, Hkv, N, d, softmax_scale, causal, o, out_dtype, lse,
                     1, nullptr, nullptr, stream);
+}
+
+fa4fp4_status fa4fp4_fwd_qbf16(const void* q, const void* kc, const void* ks, const void* vc, const void* vs,
+                               int B, int Hq, int Hkv, int N, int d, float softmax_scale, int causal, int fp8pv,
+                               void* o, int out_dtype, float* lse, void* stream) {
+  if (fp8pv != 0 && fp8pv != 1) return FA4FP4_ERR_INVALID_ARG;
+  if (!q && !(B == 0 || Hq == 0)) return FA4FP4_ERR_INVALID_ARG;
+  return fwd_common(nullptr, nullptr, kc, ks, vc, vs, B, Hq, Hkv, N, d, softmax_scale, causal, o, out_dtype, lse,
+                    fp8pv, nullptr, nullptr, stream, q);
+}
+
+fa4fp4_status fa4fp4_quantize_kv(const void* k, const void* v, int B, int Hkv, int N, int d, void* k_codes,
+                                 void* k_scales, void* vt_codes, void* vt_scales, void* stream) {
+  fa4fp4_status s = check_dims(B, Hkv, Hkv, N, d);
+  if (s != FA4FP4_OK) return s;
+  if (B == 0 || Hkv == 0) return FA4FP4_OK;
+  const void* ptrs[] = {k, v, k_codes, k_scales, vt_codes, vt_scales};
+  for (const void* ptr : ptrs)
+    if (!ptr) return FA4FP4_ERR_INVALID_ARG;
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return FA4FP4_ERR_ALIGNMENT;
+  // the Q/K/V launch with no Q rows: its row CTAs all take K
+  return launch_status(launch_quantize_qkv(nullptr, k, v, 0, (long long)B * Hkv, N, d, nullptr, nullptr, k_codes,
+                                           k_scales, vt_codes, vt_scales, static_cast<cudaStream_t>(stream)));
 }
 
 fa4fp4_status fa4fp4_fwd_nvfp4(const void* qc, const void* qs, const float* q_ts, const void* kc,

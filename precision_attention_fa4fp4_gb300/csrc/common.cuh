@@ -358,6 +358,39 @@ FA4_DEV uint32_t pack_e4m3x4(float x0, float x1, float x2, float x3) {
   return out;
 }
 
+// One MXFP4 block (OCP MX rule) of 32 bf16 values given as four 16-byte words
+// (element 2i in the low half of word i/2): amax, exponent X = E(amax) - 127 -
+// 2 clamped to [-127, 127], elements x * 2^-X (exact) rounded to E2M1 (nearest
+// even, saturating).  Returns the scale byte X + 127; the 32 codes go to
+// `codes` (element 2i in the low nibble of byte i).  The one routine behind
+// every MXFP4 quantization along d (the quantize kernels and the forward's
+// bf16-Q prologue), so both give identical bytes.
+FA4_DEV uint32_t mxfp4_block32_bf16(const uint4 (&v)[4], uint4& codes) {
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[i * 8 + 2 * j] = __uint_as_float(w[j] << 16);
+      f[i * 8 + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  int X = (int)((__float_as_uint(amax) >> 23) & 0xff) - 127 - 2;
+  X = X < -127 ? -127 : (X > 127 ? 127 : X);
+  const float inv = __uint_as_float((uint32_t)(127 - X) << 23);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) f[i] *= inv;
+  codes.x = pack_e2m1x8(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]);
+  codes.y = pack_e2m1x8(f[8], f[9], f[10], f[11], f[12], f[13], f[14], f[15]);
+  codes.z = pack_e2m1x8(f[16], f[17], f[18], f[19], f[20], f[21], f[22], f[23]);
+  codes.w = pack_e2m1x8(f[24], f[25], f[26], f[27], f[28], f[29], f[30], f[31]);
+  return (uint32_t)(X + 127);
+}
+
 // 2^e as a float for integer e in [-126, 127].
 FA4_DEV float exp2i(int e) { return __int_as_float((e + 127) << 23); }
 

@@ -168,7 +168,11 @@ FA4_DEV void stage_sf_rows(uint8_t* chunk, const uint8_t* src, int row0, int nro
   *reinterpret_cast<uint4*>(chunk + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-template <int D, bool P8, bool NV>
+// QBF: Q arrives as bf16 and the softmax warps quantize it to MXFP4 in the
+// kernel's prologue (one thread per query row, straight into the swizzled Q
+// tiles and their scale chunks), so an inference step needs no separate pass
+// over Q; K and V^T arrive quantized.
+template <int D, bool P8, bool NV, bool QBF>
 __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_constant__ FwdFp4Params p) {
   using L = Layout<D, P8, NV>;
   constexpr int NSC = L::NSC, QSB = L::QSB;
@@ -208,7 +212,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
   const int nt = p.causal ? min(nk_all, 2 * pair + 2) : nk_all;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    mbar_init(q_full, QBF ? NSOFT : 1);   // bf16 Q: one arrival per softmax warp
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1);
       mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1);
@@ -260,7 +264,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
     // tiles, so that the tile loads are not held behind them; the 2-byte
     // words of d = 64 by plain loads
     const uint8_t* qs = p.q_scales + (long long)bh * p.N * QSB;
-    if constexpr (QSB >= 4) {
+    if constexpr (QBF) {
+      // Q is quantized by the softmax warps
+    } else if constexpr (QSB >= 4) {
 #pragma unroll
       for (int x = 0; x < 2; ++x)
 #pragma unroll
@@ -283,7 +289,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       fence_proxy_async_smem();
     }
     __syncwarp();
-    if (lane == 0) {
+    if (!QBF && lane == 0) {
       mbar_arrive_expect_tx(q_full, 2 * L::QB);
       tma_load_3d(smem + L::OFF_Q, &p.tm_q, q_full, 0, q0, bh);
       tma_load_3d(smem + L::OFF_Q + L::QB, &p.tm_q, q_full, 0, q0 + BM, bh);
@@ -482,6 +488,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
     // swizzle phase of row r: 64-byte rows (E2M1) or 128-byte rows (E4M3)
     const int sw = P8 ? (r & 7) : ((r >> 1) & 3);
     uint8_t* prow = smem + L::OFF_P + 2 * x * L::PB + r * L::PROW;
+    if constexpr (QBF) {
+      // prologue: this thread's bf16 Q row to MXFP4 (blocks of 32 along d),
+      // the codes into the swizzled row of the Q tile (64-byte rows with the
+      // 64-byte swizzle at d = 128, 32-byte rows with the 32-byte swizzle at
+      // d = 64), the d/32 scale bytes into the tile's scale chunk; rows past
+      // N hold zeros, as the tile load would give them
+      uint8_t* qrow = smem + L::OFF_Q + x * L::QB + r * (D / 2);
+      uint32_t sword = 0;
+      uint4 code[D / 32];
+      if (qi < p.N) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.q_bf16) + ((long long)bh * p.N + qi) * (D / 8);
+        uint4 v[D / 32][4];
+#pragma unroll
+        for (int kb = 0; kb < D / 32; ++kb)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) v[kb][i] = __ldg(src + 4 * kb + i);
+#pragma unroll
+        for (int kb = 0; kb < D / 32; ++kb) sword |= mxfp4_block32_bf16(v[kb], code[kb]) << (8 * kb);
+      } else {
+#pragma unroll
+        for (int kb = 0; kb < D / 32; ++kb) code[kb] = make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int kb = 0; kb < D / 32; ++kb) {
+        const int cs = D == 128 ? (kb ^ ((r >> 1) & 3)) : (kb ^ ((r >> 2) & 1));
+        *reinterpret_cast<uint4*>(qrow + 16 * cs) = code[kb];
+      }
+      *reinterpret_cast<uint32_t*>(smem + L::SF_Q + x * 512 + (r % 32) * 16 + (r / 32) * 4) = sword;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_full);
+    }
     float m = -INFINITY;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
@@ -672,12 +710,12 @@ __global__ void directp_codes_kernel(const float* __restrict__ s, long long n, f
 
 }  // namespace
 
-template <int D, bool P8, bool NV>
+template <int D, bool P8, bool NV, bool QBF = false>
 static cudaError_t launch_fwd_t(const FwdFp4Params& p, cudaStream_t st) {
   using L = Layout<D, P8, NV>;
   const int nq = (p.N + BM - 1) / BM;
   const dim3 grid = p.causal ? dim3(p.B * p.Hq, (nq + 1) / 2) : dim3((nq + 1) / 2, p.B * p.Hq);
-  auto k = fwd_fp4_kernel<D, P8, NV>;
+  auto k = fwd_fp4_kernel<D, P8, NV, QBF>;
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
   k<<<grid, NTHREADS, L::BYTES, st>>>(p);
   return cudaGetLastError();
@@ -685,6 +723,10 @@ static cudaError_t launch_fwd_t(const FwdFp4Params& p, cudaStream_t st) {
 
 cudaError_t launch_fwd_fp4(const FwdFp4Params& p, cudaStream_t st) {
   const bool nv = p.ts_q != nullptr;
+  if (p.q_bf16) {   // MXFP4 Q quantized in the forward's prologue
+    if (p.fp8pv) return p.d == 128 ? launch_fwd_t<128, true, false, true>(p, st) : launch_fwd_t<64, true, false, true>(p, st);
+    return p.d == 128 ? launch_fwd_t<128, false, false, true>(p, st) : launch_fwd_t<64, false, false, true>(p, st);
+  }
   if (p.fp8pv) {
     if (nv) return p.d == 128 ? launch_fwd_t<128, true, true>(p, st) : launch_fwd_t<64, true, true>(p, st);
     return p.d == 128 ? launch_fwd_t<128, true, false>(p, st) : launch_fwd_t<64, true, false>(p, st);

@@ -50,6 +50,7 @@ struct FwdFp4Params {
   int fp8pv;                        // 0: Direct-P (E2M1 P); 1: FP8 P/V route (E4M3 P and V)
   const float* ts_q;                // NVFP4 Q/K: device tensor scales; nullptr for MXFP4 Q/K
   const float* ts_k;
+  const void* q_bf16;               // bf16 Q quantized in the kernel's prologue (tm_q unused), or nullptr
   float scale, c;                   // softmax scale, fl32(scale*log2 e)
   float T[7];                       // Direct-P thresholds
 };

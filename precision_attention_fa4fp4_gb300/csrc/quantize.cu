@@ -38,6 +38,12 @@ FA4_DEV int block_exp(float amax, float* inv) {
 template <int FMT>
 FA4_DEV void quant_row_block_v(const uint4 (&v)[4], long long b, uint8_t* __restrict__ codes,
                                uint8_t* __restrict__ scales) {
+  if constexpr (FMT == 0) {
+    uint4 o;
+    scales[b] = (uint8_t)mxfp4_block32_bf16(v, o);
+    reinterpret_cast<uint4*>(codes)[b] = o;
+    return;
+  }
   float f[32];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {

@@ -78,6 +78,13 @@ def test_argument_errors_before_launch(lib):
     assert lib.fa4fp4_quantize_qkv(*qkv, 1, 4, 2, 64, 96, *outs, null) == UNSUP      # d
     assert lib.fa4fp4_quantize_qkv(p, p, odd, 1, 4, 2, 64, 64, *outs, null) == ALIGN
     assert lib.fa4fp4_quantize_qkv(*qkv, 1, 4, 2, 64, 64, *([p] * 4 + [odd, p]), null) == ALIGN
+    assert lib.fa4fp4_fwd_qbf16(null, p, p, p, p, 1, 4, 2, 64, 64, 0.0, 0, 0, p, 1, null, null) == INVALID
+    assert lib.fa4fp4_fwd_qbf16(p, p, p, p, p, 1, 4, 2, 64, 64, 0.0, 0, 2, p, 1, null, null) == INVALID  # fp8pv
+    assert lib.fa4fp4_fwd_qbf16(p, p, p, p, p, 1, 4, 3, 64, 64, 0.0, 0, 0, p, 1, null, null) == UNSUP
+    assert lib.fa4fp4_fwd_qbf16(odd, p, p, p, p, 1, 4, 2, 64, 64, 0.0, 0, 0, p, 1, null, null) == ALIGN
+    assert lib.fa4fp4_quantize_kv(null, p, 1, 2, 64, 64, p, p, p, p, null) == INVALID
+    assert lib.fa4fp4_quantize_kv(p, p, 1, 2, 64, 96, p, p, p, p, null) == UNSUP
+    assert lib.fa4fp4_quantize_kv(p, p, 1, 2, 64, 64, p, p, odd, p, null) == ALIGN
     assert lib.fa4fp4_directp_codes(null, 10, 0.0, 1.0, 0, p, null) == INVALID
     assert lib.fa4fp4_directp_codes(p, 10, 0.0, 1.0, 2, p, null) == INVALID
     assert lib.fa4fp4_status_string(5).decode() == "device pipeline wait timed out"
@@ -106,6 +113,8 @@ def test_empty_problems_are_noops(lib):
         assert lib.fa4fp4_fwd_fp8pv(*n6, B, H, Hkv, 300, 64, 0.0, 0, null, 0, null, null) == OK
         assert lib.fa4fp4_fwd_nvfp4(*([null] * 8), B, H, Hkv, 300, 128, 0.0, 1, 1, null, 1, null, null) == OK
         assert lib.fa4bf16_fwd(null, null, null, B, H, Hkv, 300, 128, 0.0, 1, null, 1, null, null) == OK
+        assert lib.fa4fp4_fwd_qbf16(*([null] * 5), B, H, Hkv, 300, 128, 0.0, 1, 0, null, 1, null, null) == OK
+        assert lib.fa4fp4_quantize_kv(null, null, B, Hkv, 300, 128, null, null, null, null, null) == OK
         assert lib.fa4fp4_bwd(*([null] * 11), 0, null, null, B, H, Hkv, 300, 128, 0.0, 1,
                               null, null, null, null, 0, null) == OK
         assert lib.fa4fp4_bwd_workspace_bytes(B, H, Hkv, 300, 128) == 0

@@ -105,3 +105,23 @@ def test_quantize_nvfp4_refuses_wrong_out():
                        torch.zeros(B, Hkv, N, d // 32, dtype=torch.uint8), torch.ones(1), (B, Hkv, N, d))
     with pytest.raises(ValueError, match="out: codes/scales/ts"):
         api.quantize_nvfp4(x, out=bad)
+
+
+def test_fwd_qbf16_and_quantize_kv_check_buffers():
+    _, k4, vt = fwd_inputs()
+    q = torch.zeros(B, Hq, N, d, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        api.fwd_qbf16(q, k4, vt)
+    with pytest.raises(ValueError, match="bf16"):
+        api.fwd_qbf16(q.float(), k4, vt)
+    with pytest.raises(ValueError, match="vt: expected"):
+        api.fwd_qbf16(q, k4, qt(Hkv, api.FMT_MXFP4, api.ALONG_D))
+    with pytest.raises(ValueError, match="k: codes/scales"):
+        api.fwd_qbf16(q, qt(Hkv, api.FMT_MXFP4, api.ALONG_D, n=N - 1), vt)
+    k = torch.zeros(B, Hkv, N, d, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        api.quantize_kv(k, k)
+    with pytest.raises(ValueError, match="same shape"):
+        api.quantize_kv(k, torch.zeros(B, Hkv, N - 1, d, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="out\\[1\\]"):
+        api.quantize_kv(k, k, out=(qt(Hkv, api.FMT_MXFP4, api.ALONG_D), qt(Hkv, api.FMT_MXFP4, api.ALONG_D)))
