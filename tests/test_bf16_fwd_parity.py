@@ -56,3 +56,13 @@ def test_video_dit_sampled():
 @pytest.mark.parametrize("w", [SWEEP[0], SWEEP[5], SWEEP[11]], ids=lambda w: w.name)
 def test_sweep_points_sampled(w):
     check(w, rows=sample_rows(w, tiles_per_head=2, heads=[w.B * w.Hq - 1]))
+
+
+@pytest.mark.parametrize("B,Hq,Hkv", [(2, 3, 3), (1, 8, 1), (2, 6, 2)], ids=["mha", "mqa", "gqa3"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [257, 300])
+def test_head_groupings(B, Hq, Hkv, causal, N):
+    """kv head = h / (Hq / Hkv) across batches; N = 257 and 300 leave the last
+    pair of query tiles with one partial tile (the other past N)."""
+    check(Workload(f"bf16_heads_b{B}_hq{Hq}_hkv{Hkv}_n{N}", B, Hq, Hkv, N, 128, causal=causal),
+          seed=B * 100 + Hq * 10 + Hkv + N)
