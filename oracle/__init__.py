@@ -54,6 +54,7 @@ def _load():
             lib.orc_e8m0_value.restype = ctypes.c_double
             lib.orc_round_to_code.argtypes = [ctypes.c_double, c_int]
             lib.orc_block_exponent.argtypes = [c_float, c_int]
+            lib.orc_p_block_exponent.argtypes = [c_float]
             lib.orc_quantize.argtypes = [fp, c_int, c_int, c_int, c_int, c_int, c_int, u8, u8]
             lib.orc_dequantize.argtypes = [u8, u8, c_int, c_int, c_int, c_int, c_int, c_int, fp]
             lib.orc_directp_thresholds.argtypes = [fp]
@@ -109,6 +110,12 @@ def round_to_code(y: float, fmt: int) -> int:
 
 def block_exponent(amax: float, fmt: int) -> int:
     return int(_load().orc_block_exponent(float(amax), int(fmt)))
+
+
+def p_block_exponent(amax: float) -> int:
+    """E8M0 exponent of an E4M3 probability block: the smallest X with
+    amax <= 448 * 2^X (no saturation), clamped to [-127, 127]."""
+    return int(_load().orc_p_block_exponent(float(amax)))
 
 
 # --------------------------------------------------------------------------

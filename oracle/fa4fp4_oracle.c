@@ -112,6 +112,20 @@ ORC_API int orc_block_exponent(float amax, int fmt) {
     return X;
 }
 
+/* Block exponent of an E4M3 probability block (P of the FP8 P/V forward and
+ * of the backward): the smallest X with amax <= 448 * 2^X, i.e.
+ * X = ceil(log2(amax / 448)), clamped to the E8M0 range.  It is the OCP
+ * exponent, or one more where the OCP exponent would put amax above 448.
+ * Reading: the pages fix no scale rule.  Under the OCP rule a block maximum
+ * whose significand is above 1.75 saturates to 448 (up to 12.5 % low), and
+ * a probability 1 computed a few ulps low (a row with one key) falls to
+ * 0.875 while exactly 1 stays 1; this rule has neither effect. */
+ORC_API int orc_p_block_exponent(float amax) {
+    int X = orc_block_exponent(amax, 1);
+    if (X < 127 && (double)amax > ldexp(448.0, X)) X += 1;
+    return X;
+}
+
 /* Quantize a logical [B,H,N,d] FP32 tensor (holding bf16 values) in blocks of
  * 32 along one axis.
  *   fmt  : 0 = MXFP4 (E2M1 codes, two per byte, element 2i in the low nibble)
@@ -358,16 +372,16 @@ ORC_API void orc_directp_codes_of_x(const float* x, long n, uint8_t* out) {
  *   summary: the retained training route keeps FP8 probabilities and values):
  *   s and the running max as in mode 0; p = fl32(2^x) with x =
  *   fl32(fl32(s - m_j) * c) (the difference first: it is exact near the max,
- *   so the row max gets x = 0 and p = 1 exactly, never the value just below
- *   1 that the E4M3 block rule would saturate); p rounded through MXFP8
- *   (E4M3 with one E8M0 scale per 32
- *   keys, blocks aligned to absolute key positions 32a) as the P V operand;
+ *   so the row max gets x = 0 and p = 1 exactly); p rounded to E4M3 with one
+ *   E8M0 scale per 32 keys from orc_p_block_exponent (blocks aligned to
+ *   absolute key positions 32a) as the P V operand;
  *   l <- alpha*l + sum deq(p8) (the normalizer from the same rounded values
  *   the product consumes); O <- alpha*O + sum deq(p8)*V, V being the
  *   dequantized MXFP8 V.  Output O/l, LSE = scale*m + ln l.
  * Causal: key n is valid for query i iff n <= i; key tiles wholly above the
  * diagonal are skipped. */
 static void mxfp8_roundtrip(double* v, int n, long stride);
+static void p_e4m3_roundtrip(double* v, int n);
 ORC_API void orc_fwd(const float* Q, const float* K, const float* V, int B, int Hq, int Hkv,
                      int N, int d, float softmax_scale, int causal, int mode, long nrows,
                      const int64_t* rows, double* O_out, double* LSE_out) {
@@ -410,7 +424,7 @@ ORC_API void orc_fwd(const float* Q, const float* K, const float* V, int B, int 
             for (int t = 0; t < d; ++t) o[t] *= alpha;
             if (mode == 2) {
                 /* p = fl32(2^x), x = fl32(fl32(s - m) * c), for the valid keys,
-                 * then MXFP8 in 32-key blocks */
+                 * then E4M3 in 32-key blocks under orc_p_block_exponent */
                 for (int n = 0; n < cnt; ++n) {
                     const float dx = (float)s[n] - (float)mnew;
                     const float x = dx * c;
@@ -418,7 +432,7 @@ ORC_API void orc_fwd(const float* Q, const float* K, const float* V, int B, int 
                 }
                 for (int a0 = 0; a0 < cnt; a0 += 32) {
                     int nb = cnt - a0 < 32 ? cnt - a0 : 32;
-                    mxfp8_roundtrip(s + a0, nb, 1);
+                    p_e4m3_roundtrip(s + a0, nb);
                 }
             }
             for (int n = 0; n < cnt; ++n) {
@@ -459,6 +473,21 @@ static void mxfp8_roundtrip(double* v, int n, long stride) {
     }
 }
 
+/* E4M3 round trip of one block of probabilities v[0..n) (n <= 32, the rest
+ * of the block counts as zero) under orc_p_block_exponent. */
+static void p_e4m3_roundtrip(double* v, int n) {
+    float amax = 0.0f;
+    for (int t = 0; t < n; ++t) {
+        float a = fabsf((float)v[t]);
+        if (a > amax) amax = a;
+    }
+    int X = orc_p_block_exponent(amax);
+    for (int t = 0; t < n; ++t) {
+        double y = ldexp((double)(float)v[t], -X);
+        v[t] = ldexp(orc_e4m3_value(orc_round_to_code(y, 1)), X);
+    }
+}
+
 /* Gradients of the forward above for a chosen set of rows.
  *
  * Inputs (logical [B,H,N,d] float arrays):
@@ -473,8 +502,8 @@ static void mxfp8_roundtrip(double* v, int n, long stride) {
  *   dO is quantized twice: blocks along d (row view, feeds dP) and blocks of
  *   32 queries (column view, feeds dV);
  *   dP = dO_row . V8;  dS = P*(dP - D) with the FP32 P;
- *   Pq: P in blocks of 32 queries; dS_row: blocks of 32 keys; dS_col: blocks
- *   of 32 queries;
+ *   Pq: P in blocks of 32 queries, E4M3 under orc_p_block_exponent; dS_row:
+ *   blocks of 32 keys; dS_col: blocks of 32 queries (MXFP8, OCP rule);
  *   dV = sum_q Pq^T dO_col;  dK = scale * sum_q dS_col^T Q8;
  *   dQ = scale * sum_k dS_row K8; dK, dV summed over a GQA group.
  *   Blocks of 32 are aligned to absolute positions 32a and cover masked or
@@ -614,7 +643,7 @@ ORC_API void orc_bwd(const float* Q4, const float* K4, const float* Q8, const fl
                     for (int t = 0; t < d; ++t) dOcol[u * d + t] = dO[off + t];
                 }
                 if (mode == 0) {
-                    mxfp8_roundtrip(Pb, 32, 1);
+                    p_e4m3_roundtrip(Pb, 32);
                     mxfp8_roundtrip(dSb, 32, 1);
                     for (int t = 0; t < d; ++t) mxfp8_roundtrip(dOcol + t, 32, d);
                 }

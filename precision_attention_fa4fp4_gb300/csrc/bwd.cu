@@ -448,11 +448,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
           }
         }
       }
-      // P and dS in blocks of 32 queries (this thread's columns)
+      // P and dS in blocks of 32 queries (this thread's columns); P under the
+      // probability blocks' exponent, dS under the OCP one
       float inv;
       uint4 lo, hi;
-      const int xp = e4m3_block_exp(pmax, &inv);
-      e4m3x32(s, inv, lo, hi);
+      const int xp = e4m3_p_block_exp(pmax);
+      e4m3x32(s, __uint_as_float((uint32_t)(127 - xp) << 23), lo, hi);
       st_row_sw64(pq, r, g, lo, hi);
       const int xc = e4m3_block_exp(dsmax, &inv);
       e4m3x32(dp, inv, lo, hi);

@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
       if constexpr (P8) {
         // p = 2^x with x = fl32(fl32(s - m) * c) (exact difference near the
         // max: the row max gets p = 1 exactly), then E4M3 with one E8M0 scale
-        // per 32 keys (OCP MX rule: X = E(amax) - 127 - 8); the row's four
+        // per 32 keys (the least X with amax <= 448 * 2^X); the row's four
         // scale bytes go to the scale-factor chunk of this tile and step
         uint32_t sfw = 0;
 #pragma unroll
@@ -568,8 +568,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
             s[g][i + 1] = ex2_approx(xx.y);
             amax = fmax3(amax, s[g][i], s[g][i + 1]);
           }
-          int X = (int)((__float_as_uint(amax) >> 23) & 0xff) - 127 - 8;
-          X = X < -127 ? -127 : (X > 127 ? 127 : X);
+          const int X = e4m3_p_block_exp(amax);
           const float inv = __uint_as_float((uint32_t)(127 - X) << 23);
           sfw |= (uint32_t)(X + 127) << (8 * g);
           uint32_t w[8];

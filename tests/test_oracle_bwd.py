@@ -150,7 +150,7 @@ def test_mode0_within_fp8_bound():
 # equal values along the stated one: blocked along the stated axis it is
 # exact, blocked along the other it shares an E8M0 scale with a value 2^20
 # larger and flushes to zero (E4M3's smallest subnormal is 2^-9 of the
-# block's scale, and the scale puts the block maximum in [256, 512)).  The
+# block's scale, and the scale puts the block maximum in [224, 512)).  The
 # expected gradients are written out by hand; softmax_scale = fl32(ln 2)
 # makes c = 1, so P = 2^s exactly with LSE = 0.
 # ---------------------------------------------------------------------------
@@ -220,3 +220,27 @@ def test_mxfp8_block_axes(which):
         np.testing.assert_array_equal(dK[1], SCALE_C1 * 64 * 64 * TINY * ones)
         np.testing.assert_array_equal(dK[0], SCALE_C1 * 64 * 64 * ones)
         np.testing.assert_array_equal(dK[2:], 0)
+
+
+def test_p_one_ulp_below_one_keeps_its_value():
+    """P of every query against key 0 is fl32(2^(-2^-22)) = 1 - 3*2^-24, a
+    probability 1 computed a few ulps low.  The probability blocks' exponent
+    (the least X with amax <= 448 * 2^X) scales it to 256 - 3*2^-16, which
+    rounds to 256: dV_0 = sum over 64 queries of 1 * dO = 64 exactly.  (The
+    OCP exponent, one lower, would scale it to 512 - 3*2^-15 and saturate it
+    to 448: dV_0 = 56.)"""
+    N, d = 64, 64
+    z = lambda: np.zeros((1, 1, N, d), np.float32)
+    Q4, K4, Q8, K8, V8, O, dO = z(), z(), z(), z(), z(), z(), z()
+    Q4[..., 0] = 1.0
+    K4[0, 0, :, 0] = -200.0
+    K4[0, 0, 0, 0] = -(2.0 ** -22)
+    dO[:] = 1.0
+    p = np.float32(2.0 ** -(2.0 ** -22))
+    assert p == np.float32(1 - 3 * 2.0 ** -24) and p < 1
+    dQ, dK, dV = oracle.bwd(Q4, K4, Q8, K8, V8, O, dO, np.zeros((1, 1, N), np.float32),
+                            softmax_scale=SCALE_C1, causal=False, mode=0)
+    np.testing.assert_array_equal(dV[0], 64 * np.ones(d))
+    np.testing.assert_array_equal(dV[1:], 0)
+    np.testing.assert_array_equal(dQ, 0)
+    np.testing.assert_array_equal(dK, 0)

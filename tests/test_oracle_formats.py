@@ -4,6 +4,8 @@ Each check compares the oracle with something other than itself: the format
 definitions (bit fields), a library conversion (torch float8_e4m3fn), an
 independent binade-wise round-half-even, or an invariant of the OCP MX rule.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -113,6 +115,25 @@ def test_block_exponent_closed_form(fmt, lo, hi):
         r = float(amax) * 2.0 ** -X
         assert lo <= r < hi
     assert oracle.block_exponent(0.0, fmt) == -127
+
+
+def test_p_block_exponent_is_smallest_unsaturated():
+    """The probability blocks' exponent is the least X with amax <= 448 * 2^X
+    (checked by exact double comparisons, and against the OCP exponent: the
+    same below a significand of 1.75, one more above it)."""
+    g = np.random.default_rng(1)
+    a = np.float32(np.abs(g.standard_normal(5000)) * np.exp2(g.integers(-60, 60, 5000))) + np.float32(1e-30)
+    edge = np.float32([1.0, np.nextafter(np.float32(1), np.float32(0)), 0.875, 0.95, 1.75, 0.5,
+                       np.nextafter(np.float32(0.875), np.float32(1)), 448.0, 449.0])
+    for amax in np.concatenate([a, edge]):
+        X = oracle.p_block_exponent(float(amax))
+        assert float(amax) <= math.ldexp(448.0, X) and float(amax) > math.ldexp(448.0, X - 1)
+        frac = math.frexp(float(amax))[0] * 2     # significand in [1, 2)
+        assert X == oracle.block_exponent(float(amax), 1) + (1 if frac > 1.75 else 0)
+    # one ulp below 1 takes the exponent of 1 (1 - 2^-24 scales to 256 - 2^-16,
+    # which rounds to the E4M3 value 256)
+    assert oracle.p_block_exponent(float(edge[1])) == oracle.p_block_exponent(1.0) == -8
+    assert oracle.p_block_exponent(0.0) == -127
 
 
 @pytest.mark.parametrize("fmt", [0, 1])

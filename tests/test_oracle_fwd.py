@@ -222,6 +222,28 @@ def test_fp8pv_scale_per_32_keys():
     assert abs(O2[0, 0] - 1.0) > 0.9                 # not flushed
 
 
+def test_fp8pv_block_max_above_1_75_not_saturated():
+    """Keys 0-31 have p = 1 (the max, V = 0), keys 32-63 p ~ 0.95 (V = 1 in
+    channel 0), c = 1.  The second block's maximum has significand 1.9: its
+    exponent is the least X with 0.95 <= 448 * 2^X, X = -8, so p scales to
+    243.2 and rounds to the E4M3 value 240: O[0] = (240/256) / (1 + 240/256)
+    and LSE = ln(32 + 32 * 240/256).  (Under the OCP exponent, X = -9, it
+    would saturate to 448/512 = 0.875.)"""
+    d, N = 64, 64
+    scale = float(np.float32(np.log(2.0)))          # c = fl32(scale * log2 e) = 1
+    Q = np.zeros((1, 1, N, d), np.float32)
+    Q[0, 0, 0, 0] = 1.0
+    K = np.zeros((1, 1, N, d), np.float32)
+    K[0, 0, 32:, 0] = np.float32(np.log2(0.95))
+    V = np.zeros((1, 1, N, d), np.float32)
+    V[0, 0, 32:, 0] = 1.0
+    O, L = oracle.fwd(Q, K, V, softmax_scale=scale, mode=2, rows=np.arange(1))
+    p8 = 240.0 / 256.0
+    assert abs(O[0, 0] - p8 / (1 + p8)) < 1e-12
+    np.testing.assert_array_equal(O[0, 1:], 0)
+    assert abs(L[0] - np.log(32 + 32 * p8)) < 1e-6
+
+
 def test_fp8pv_permutation_within_32_key_blocks():
     d, N = 64, 300
     Qd, Kd, Vd = quantized_inputs(rand((1, 2, N, d), 34), rand((1, 2, N, d), 35), rand((1, 2, N, d), 36))
