@@ -107,11 +107,22 @@ FA4_DEV void stage_chunk(uint8_t* chunk, const uint8_t* src, long long stride, i
 // 32 floats * inv -> 32 E4M3 codes as two uint4 (element 0 in byte 0)
 FA4_DEV void e4m3x32(const float* v, float inv, uint4& lo, uint4& hi) {
   uint32_t w[8];
+  const float2 f = make_float2(inv, inv);
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    w[i] = pack_e4m3x4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+  for (int i = 0; i < 8; ++i) {
+    const float2 a = fmul2(make_float2(v[4 * i], v[4 * i + 1]), f);
+    const float2 b = fmul2(make_float2(v[4 * i + 2], v[4 * i + 3]), f);
+    w[i] = pack_e4m3x4(a.x, a.y, b.x, b.y);
+  }
   lo = make_uint4(w[0], w[1], w[2], w[3]);
   hi = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// max |v| over the 32 lanes of the warp
+FA4_DEV float warp_max_abs(float v) {
+  float r;
+  asm volatile("redux.sync.max.abs.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
 
 // two 16-byte chunks 2g, 2g+1 of row r of a [rows][64 B] SW64 tile
@@ -465,17 +476,41 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
       // of the column's amax (sign bit clear): X = max(E - 135, -127), so the
       // factor 2^-X has exponent field min(262 - E, 254) and the scale byte is
       // X + 127 = max(E, 8) - 8.
-      float q8[32];
-      uint32_t my_e = 0;
+      // The column maxima are warp-uniform: their exponent bytes are packed
+      // four to a word, and each lane picks its own column's at the end.
+      uint32_t ew[8];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const uint32_t E = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(dp[i]))) >> 23;
-        q8[i] = dp[i] * __uint_as_float(min(262u - E, 254u) << 23);
-        my_e = lane == i ? E : my_e;
+      for (int i = 0; i < 32; i += 4) {
+        uint32_t eb[4];
+#pragma unroll
+        for (int u = 0; u < 4; u += 2) {
+          const uint32_t a0 = __float_as_uint(warp_max_abs(dp[i + u]));
+          const uint32_t a1 = __float_as_uint(warp_max_abs(dp[i + u + 1]));
+          const float2 f = make_float2(__uint_as_float(min(0x83000000u - (a0 & 0x7f800000u), 0x7f000000u)),
+                                       __uint_as_float(min(0x83000000u - (a1 & 0x7f800000u), 0x7f000000u)));
+          const float2 qv = fmul2(make_float2(dp[i + u], dp[i + u + 1]), f);
+          dp[i + u] = qv.x;
+          dp[i + u + 1] = qv.y;
+          eb[u] = a0 << 1;          // E in byte 3
+          eb[u + 1] = a1 << 1;
+        }
+        ew[i / 4] = __byte_perm(__byte_perm(eb[0], eb[1], 0x0073), __byte_perm(eb[2], eb[3], 0x0073), 0x5410);
       }
-      e4m3x32(q8, 1.f, lo, hi);
-      st_row_sw64(dsr, r, g, lo, hi);
-      sfc[(7 + sp) * 512 + lane * 16 + g * 4 + quad] = (uint8_t)(max(my_e, 8u) - 8u);
+      {
+        uint32_t pair_lo, pair_hi;   // words 2k, 2k+1 with k = lane / 8
+        const uint32_t l0 = (lane & 8) ? ew[2] : ew[0], h0 = (lane & 8) ? ew[3] : ew[1];
+        const uint32_t l1 = (lane & 8) ? ew[6] : ew[4], h1 = (lane & 8) ? ew[7] : ew[5];
+        pair_lo = (lane & 16) ? l1 : l0;
+        pair_hi = (lane & 16) ? h1 : h0;
+        const uint32_t my_e = __byte_perm(pair_lo, pair_hi, (uint32_t)(lane & 7)) & 0xffu;
+        sfc[(7 + sp) * 512 + lane * 16 + g * 4 + quad] = (uint8_t)(max(my_e, 8u) - 8u);
+      }
+      {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = pack_e4m3x4(dp[4 * i], dp[4 * i + 1], dp[4 * i + 2], dp[4 * i + 3]);
+        st_row_sw64(dsr, r, g, make_uint4(w[0], w[1], w[2], w[3]), make_uint4(w[4], w[5], w[6], w[7]));
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[sp]);
