@@ -11,9 +11,9 @@
  * saved quantized Q and K and uses FP8 E4M3 operands.
  *
  * Conventions shared by every call:
- *   - Pointers are DEVICE pointers, allocated and owned by the caller.  The
- *     library never allocates or frees memory and never synchronizes, except
- *     in fa4fp4_sync_status.
+ *   - Pointers are DEVICE pointers, allocated and owned by the caller, except
+ *     the host buffers of fa4fp4_fwd_host.  The library never allocates or
+ *     frees memory and never synchronizes, except in fa4fp4_sync_status.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Every compute call is asynchronous on it; the return value
  *     reports host-side argument validation and launch errors only.  Device
@@ -115,6 +115,35 @@ FA4FP4_API fa4fp4_status fa4fp4_fwd(const void* q_codes, const void* q_scales, c
                          int B, int Hq, int Hkv, int N, int d, float softmax_scale, int causal,
                          void* o, int out_dtype, float* lse, void* stream);
 
+/* The inference step end to end on HOST buffers: bf16 q [B][Hq][N][d] and k,
+ * v [B][Hkv][N][d] in host memory, o (f32 or bf16 per out_dtype,
+ * [B][Hq][N][d]) and lse (nullable, f32 [B][Hq][N]) written to host memory;
+ * on the device, fa4fp4_quantize_qkv and fa4fp4_fwd (technical summary,
+ * Methodology 1: MXFP4 Q, K, V and the Direct-P forward), with the same
+ * results as those two calls on the same data.  The pages have no
+ * counterpart; this is the library's end-to-end entry point.  The work is cut
+ * into chunks of (batch element, range of kv heads) with their query heads;
+ * each chunk's inputs are copied in on an internal stream, quantized and
+ * attended on `stream`, and copied out on a second internal stream, two
+ * chunks' staging buffers in flight, so that the copies overlap the compute.
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for
+ * the copies to overlap; q, k, v, o must be 16-byte aligned and lse 4-byte
+ * aligned.  `workspace` is DEVICE memory of at least
+ * fa4fp4_fwd_host_workspace_bytes(B, Hq, Hkv, N, d) bytes, 16-byte aligned
+ * (FA4FP4_ERR_WORKSPACE if missing or too small), used as staging; calls in
+ * flight at the same time need their own workspaces.  The call is
+ * asynchronous on `stream`: later work on `stream` sees o and lse in host
+ * memory, and the call starts after earlier work on `stream`.  The first call
+ * on a device creates two streams and seven events on it, kept until the
+ * process exits.  Other errors as fa4fp4_fwd's; all checks are made before
+ * anything is enqueued, and a CUDA failure while enqueuing returns
+ * FA4FP4_ERR_CUDA with the chunks before it already enqueued. */
+FA4FP4_API size_t fa4fp4_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
+FA4FP4_API fa4fp4_status fa4fp4_fwd_host(const void* q_host, const void* k_host, const void* v_host, int B,
+                                         int Hq, int Hkv, int N, int d, float softmax_scale, int causal,
+                                         void* o_host, int out_dtype, float* lse_host, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+
 /* The FP8 P/V training route of the forward (technical summary, Methodology 2
  * "Stability Constraint" and Training Performance: the retained training route
  * keeps FP8 probabilities and values).  Same arguments, layouts and errors as
@@ -124,7 +153,8 @@ FA4FP4_API fa4fp4_status fa4fp4_fwd(const void* q_codes, const void* q_scales, c
  * in ascending order: S = Q K^T on FP4 tensor cores, running max m, p =
  * 2^x with x = fl32(fl32(s - m) c) in FP32 (hardware exponential; the row max
  * gets p = 1 exactly), P rounded to E4M3
- * with one E8M0 scale per 32 keys (OCP MX rule), O += P V and l += P 1 on
+ * with one E8M0 scale per 32 keys (the least X with amax <= 448 * 2^X, so no
+ * element saturates), O += P V and l += P 1 on
  * FP8 tensor cores (kind::mxf8f6f4), eager rescale when m grows.  Outputs
  * O / l and LSE = softmax_scale * m + ln(l). */
 FA4FP4_API fa4fp4_status fa4fp4_fwd_fp8pv(const void* q_codes, const void* q_scales, const void* k_codes,
@@ -194,7 +224,8 @@ FA4FP4_API size_t fa4fp4_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int 
  * Computes P = 2^(fmaf(s, c, -fl32(lse*log2 e))), D = rowsum(dO*O), the MXFP8
  * views of dO (blocks along d and blocks of 32 queries), dP = dO V^T, dS =
  * P*(dP-D), and, with P and dS quantized to MXFP8 (P and dS in blocks of 32
- * queries for dV/dK, dS in blocks of 32 keys for dQ):
+ * queries for dV/dK, dS in blocks of 32 keys for dQ; P's blocks take the
+ * least X with amax <= 448 * 2^X, dS's the OCP MX exponent):
  *   dV = P^T dO, dK = scale * dS^T Q, dQ = scale * dS K
  * summed over the query heads of each kv head.  dq [B][Hq][N][d], dk/dv
  * [B][Hkv][N][d], all f32, fully overwritten.  `workspace` must hold

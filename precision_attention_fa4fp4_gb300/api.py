@@ -64,6 +64,10 @@ def load_library():
         lib.fa4fp4_fwd_qbf16.argtypes = [vp] * 5 + [i, i, i, i, i, f, i, i, vp, i, vp, vp]
         lib.fa4fp4_quantize_kv.restype = i
         lib.fa4fp4_quantize_kv.argtypes = [vp, vp, i, i, i, i, vp, vp, vp, vp, vp]
+        lib.fa4fp4_fwd_host_workspace_bytes.restype = sz
+        lib.fa4fp4_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i]
+        lib.fa4fp4_fwd_host.restype = i
+        lib.fa4fp4_fwd_host.argtypes = [vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, vp, sz, vp]
         lib.fa4fp4_bwd_workspace_bytes.restype = sz
         lib.fa4fp4_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
         lib.fa4fp4_bwd.restype = i
@@ -390,6 +394,51 @@ def _expect_grads(dq, dk, dv, B, Hq, Hkv, N, d):
     _expect("dq", dq, (B, Hq, N, d), (torch.float32,))
     _expect("dk", dk, (B, Hkv, N, d), (torch.float32,))
     _expect("dv", dv, (B, Hkv, N, d), (torch.float32,))
+
+
+def fwd_host_workspace_bytes(B, Hq, Hkv, N, d) -> int:
+    return int(load_library().fa4fp4_fwd_host_workspace_bytes(B, Hq, Hkv, N, d))
+
+
+def _host(*ts):
+    for t in ts:
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError("fa4fp4: host buffers must be contiguous CPU tensors (page-locked for overlap)")
+
+
+def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+             softmax_scale: float = 0.0, out_dtype: int = OUT_BF16, with_lse: bool = True, out=None, lse=None,
+             workspace: torch.Tensor | None = None, device=None):
+    """The inference step on host buffers (fa4fp4_fwd_host): bf16 CPU q, k, v
+    in, CPU o (and lse) out, quantization and the Direct-P forward on the
+    current CUDA device and stream.  Returns (o, lse or None); they hold the
+    result once the stream has reached the end of the call."""
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("fwd_host expects [B,H,N,d] tensors")
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    _expect("q", q, (B, Hq, N, d), (torch.bfloat16,))
+    _expect("k", k, (B, Hkv, N, d), (torch.bfloat16,))
+    _expect("v", v, (B, Hkv, N, d), (torch.bfloat16,))
+    _expect_out(out, lse if with_lse else None, B, Hq, N, d, out_dtype)
+    _host(q, k, v, out, lse if with_lse else None)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty((B, Hq, N, d), dtype=torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32,
+                          pin_memory=pin)
+    if with_lse and lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, pin_memory=pin)
+    ws_bytes = fwd_host_workspace_bytes(B, Hq, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    elif workspace.dtype != torch.uint8:
+        raise ValueError("workspace: expected a uint8 tensor")
+    _cuda(workspace)
+    _check("fa4fp4_fwd_host", load_library().fa4fp4_fwd_host(
+        _ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, N, d, float(softmax_scale), int(bool(causal)), _ptr(out), out_dtype,
+        _ptr(lse) if with_lse else None, _ptr(workspace), workspace.numel(), _stream(workspace.device)))
+    return out, (lse if with_lse else None)
 
 
 def bwd_workspace_bytes(B, Hq, Hkv, N, d) -> int:

@@ -157,3 +157,36 @@ def test_noalloc_validates_like_bwd(lib):
     assert bwd_na(*([p] * 11), 0, p, p, B, Hq, Hkv, N, 128, 0.0, 1, null, p, p, null) == INVALID
     # well-formed but oversized: the scratch limit
     assert bwd_na(*([p] * 11), 0, p, p, B, Hq, Hkv, N, 128, 0.0, 1, p, p, p, null) == WORKSPACE
+
+
+def test_fwd_host_validation_and_workspace(lib):
+    """The host-buffer inference call checks shape, options, pointers,
+    alignment and its workspace before it touches the device."""
+    p = ctypes.c_void_p(4096)
+    odd = ctypes.c_void_p(4097)
+    null = None
+    OK, INVALID, UNSUP, ALIGN, WS = 0, 1, 2, 3, 6
+    fh = lib.fa4fp4_fwd_host
+    big = 1 << 40
+    # B4 Hq16 Hkv16 N4096 d128: two chunks of 8 heads per batch element; staging
+    # for two chunks of bf16 Q, K, V (8.4 MB each), two of O (f32) and LSE, and
+    # one chunk of MXFP4 Q, K, V^T codes and scales
+    want = 2 * 3 * 8 * 4096 * 128 * 2 + 2 * (8 * 4096 * 128 * 4 + 8 * 4096 * 4) + 3 * (8 * 4096 * 64 + 8 * 4096 * 4)
+    assert lib.fa4fp4_fwd_host_workspace_bytes(4, 16, 16, 4096, 128) == want
+    assert lib.fa4fp4_fwd_host_workspace_bytes(1, 24, 24, 32760, 128) > 0
+    assert lib.fa4fp4_fwd_host_workspace_bytes(1, 4, 3, 300, 128) == 0
+    assert lib.fa4fp4_fwd_host_workspace_bytes(1, 4, 2, 300, 96) == 0
+    assert lib.fa4fp4_fwd_host_workspace_bytes(0, 4, 2, 300, 128) == 0
+    n = lib.fa4fp4_fwd_host_workspace_bytes(2, 8, 2, 300, 64)
+    assert fh(null, null, null, 0, 4, 2, 300, 128, 0.0, 1, null, 1, null, null, 0, null) == OK
+    assert fh(null, null, null, 0, 4, 2, 300, 96, 0.0, 1, null, 1, null, null, 0, null) == UNSUP
+    assert fh(p, p, p, 2, 8, 3, 300, 64, 0.0, 1, p, 1, p, p, big, null) == UNSUP
+    assert fh(p, p, p, 2, 8, 2, 0, 64, 0.0, 1, p, 1, p, p, big, null) == INVALID
+    assert fh(p, p, p, 2, 8, 2, 300, 64, 0.0, 1, p, 7, p, p, big, null) == INVALID
+    assert fh(null, p, p, 2, 8, 2, 300, 64, 0.0, 1, p, 1, p, p, big, null) == INVALID
+    assert fh(p, p, p, 2, 8, 2, 300, 64, 0.0, 1, null, 1, p, p, big, null) == INVALID
+    assert fh(p, odd, p, 2, 8, 2, 300, 64, 0.0, 1, p, 1, p, p, big, null) == ALIGN
+    assert fh(p, p, p, 2, 8, 2, 300, 64, 0.0, 1, p, 1, ctypes.c_void_p(4098), p, big, null) == ALIGN
+    assert fh(p, p, p, 2, 8, 2, 300, 64, 0.0, 1, p, 1, p, null, big, null) == WS
+    assert fh(p, p, p, 2, 8, 2, 300, 64, 0.0, 1, p, 1, p, p, n - 1, null) == WS
+    assert fh(p, p, p, 2, 8, 2, 300, 64, 0.0, 1, p, 1, p, odd, n, null) == ALIGN
