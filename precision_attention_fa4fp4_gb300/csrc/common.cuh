@@ -382,11 +382,12 @@ FA4_DEV uint32_t pack_e4m3x4(float x0, float x1, float x2, float x3) {
 // amax <= 448 * 2^X, clamped to [-127, 127].  From the FP32 fields of amax
 // (sign clear): the OCP exponent E - 135, plus one where the significand is
 // above 1.75 (448 = 1.75 * 2^8), so no element saturates and a probability 1
-// computed an ulp low scales to 256 - 2^-16 -> 256, as 1 itself does.
+// computed an ulp low scales to 256 - 2^-16 -> 256, as 1 itself does.  Adding
+// 0x1fffff to the bits carries into the exponent field exactly when the
+// significand field exceeds 0x600000; E + 1 - 135 <= 121 needs no upper clamp.
 FA4_DEV int e4m3_p_block_exp(float amax) {
-  const uint32_t b = __float_as_uint(amax);
-  const int X = (int)(b >> 23) - 135 + ((b & 0x7fffffu) > 0x600000u ? 1 : 0);
-  return X < -127 ? -127 : (X > 127 ? 127 : X);
+  const int X = (int)((__float_as_uint(amax) + 0x1fffffu) >> 23) - 135;
+  return X < -127 ? -127 : X;
 }
 
 // One MXFP4 block (OCP MX rule) of 32 bf16 values given as four 16-byte words
