@@ -40,19 +40,24 @@ FP4_OVER_BF16 = 13.5 / 2.25     # nominal dense FP4 : BF16 tensor rate on GB300
 FP8_OVER_BF16 = 4.5 / 2.25
 # DRAM read + write of one fwd_fp4_kernel<128> launch on the 4K workload, from
 # one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), with the
-# SHA-256 of the kernel's source files at that capture.  The figure is
-# reported only while those files are unchanged; after any edit it reads null
-# until the kernel is captured again.
-FWD_FP4_TRAFFIC = {"bytes": 71.32e6, "sources_sha256": "0a5a4b75d172af9e51c4b39b0207b8c458da8d97700727b5a54b89e15f2494f5"}
-FWD_FP4_SOURCES = ("csrc/fwd_fp4.cu", "csrc/common.cuh", "csrc/internal.h")
+# SHA-256 of the kernel's sources at that capture: its .cu file, the shared
+# device header and its parameter block in the host header.  The figure is
+# reported only while those are unchanged; after any edit it reads null until
+# the kernel is captured again.
+FWD_FP4_TRAFFIC = {"bytes": 71.32e6, "sources_sha256": "2901c07136cbe0cf33aeabe20cb4db40fe274417184d35c1aaf81bc3a2f1b492"}
+FWD_FP4_SOURCES = ("csrc/fwd_fp4.cu", "csrc/common.cuh")
 
 
 def fwd_sources_sha256() -> str:
     import hashlib
+    import re
     h = hashlib.sha256()
+    pkg = os.path.join(ROOT, "precision_attention_fa4fp4_gb300")
     for rel in FWD_FP4_SOURCES:
-        with open(os.path.join(ROOT, "precision_attention_fa4fp4_gb300", rel), "rb") as f:
+        with open(os.path.join(pkg, rel), "rb") as f:
             h.update(f.read())
+    with open(os.path.join(pkg, "csrc", "internal.h")) as f:
+        h.update(re.search(r"struct FwdFp4Params \{.*?\n\};", f.read(), re.S).group(0).encode())
     return h.hexdigest()
 
 

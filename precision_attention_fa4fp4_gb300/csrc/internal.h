@@ -23,7 +23,8 @@ struct QkvParams {
   int N, Np;
   long long nbq, nbk;          // 32-element blocks of Q and K
   long long nq_cta, nk_cta;    // CTAs of 512 row blocks
-  long long nv;                // 128-token V tiles
+  long long nvw;               // 32-token V blocks (one warp each)
+  long long nv;                // V CTAs (8 blocks each)
   long long period;            // every period-th CTA (of the first nv) is a V tile
 };
 cudaError_t launch_quantize_qkv(const void* q, const void* k, const void* v, long long BHq, long long BHkv,

@@ -9,9 +9,10 @@
 // Per block of 32 values: amax, E8M0 exponent X = E(amax) - 127 - emax
 // (emax = 2 for E2M1, 8 for E4M3; clamped to [-127,127]), elements x*2^-X
 // converted with round-to-nearest-even and saturation by the hardware
-// converters.  The kernels are HBM-bound: 16-byte coalesced loads, one thread
-// per block for blocks along d, and a shared-memory transpose of 128-token
-// tiles for blocks along N.
+// converters.  The kernels are HBM-bound: 16-byte coalesced loads and one
+// thread per block for blocks along d; for blocks along N one warp per
+// 32-token block, each lane holding a pair of channels of every token row in
+// registers (no shared-memory transpose).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include "common.cuh"
@@ -103,85 +104,92 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
     quant_row_block<FMT>(x, b, codes, scales);
 }
 
-// blocks along N: one (b,h) x 128-token tile t0.., output transposed
-// [bh][d][Np].  Shared tile [128 tokens][d] bf16; thread (channel, 32-token
-// block) with consecutive threads on consecutive channels.  Called by the
-// whole CTA.
+// blocks along N, output transposed [bh][d][Np]: one warp per 32-token
+// block kb of one (b,h), no shared memory.  Each lane owns a pair of
+// channels per pass (two passes at d = 128): its 4-byte loads of the pair
+// from the block's 32 token rows give the warp 128 contiguous bytes of every
+// row, and the 32 values of each of its channels end up in its registers, so
+// the block maximum, the scale and the conversion are thread-local.  Tokens
+// at or past N load as zero (codes +0, scale byte 0 for an all-zero block).
 template <int FMT, int D>
-FA4_DEV void quant_col_tile(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* tile, int N, int Np,
-                            int t0, long long bh, uint8_t* __restrict__ codes,
-                            uint8_t* __restrict__ scales) {
-  const uint4* src = reinterpret_cast<const uint4*>(x + (bh * N + t0) * (long long)D);
-  const int valid = min(128, N - t0);
-  constexpr int VEC = D / 8;   // uint4 per token row
-  for (int i = threadIdx.x; i < 128 * VEC; i += blockDim.x) {
-    int tok = i / VEC;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (tok < valid) v = __ldg(src + i);
-    reinterpret_cast<uint4*>(tile)[i] = v;
-  }
-  __syncthreads();
+FA4_DEV void quant_col_block_warp(const __nv_bfloat16* __restrict__ x, long long bh, int kb, int N, int Np,
+                                  uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int lane) {
+  const int t0 = kb * 32;
+  const int valid = min(32, N - t0);
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(x) + ((bh * N + t0) * (long long)D) / 2;
   constexpr int BYTES = FMT == 0 ? 16 : 32;    // code bytes per 32-token block
-  for (int u = threadIdx.x; u < D * 4; u += blockDim.x) {
-    const int ch = u % D, kb = u / D;
-    float f[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) f[i] = __bfloat162float(tile[(kb * 32 + i) * D + ch]);
-    float amax = 0.f;
+  for (int pass = 0; pass < D / 64; ++pass) {
+    const int c0 = pass * 64 + 2 * lane;
+    uint32_t w[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
-    float inv;
-    int X = block_exp<FMT>(amax, &inv);
+    for (int i = 0; i < 32; ++i) w[i] = i < valid ? __ldg(src + (i * D + c0) / 2) : 0u;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) f[i] *= inv;
-    const long long row = bh * D + ch;
-    scales[row * (Np / 32) + t0 / 32 + kb] = (uint8_t)(X + 127);
-    uint8_t* dst = codes + row * (long long)(Np * BYTES / 32) + (t0 / 32 + kb) * BYTES;
-    if (FMT == 0) {
-      uint4 o;
-      o.x = pack_e2m1x8(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]);
-      o.y = pack_e2m1x8(f[8], f[9], f[10], f[11], f[12], f[13], f[14], f[15]);
-      o.z = pack_e2m1x8(f[16], f[17], f[18], f[19], f[20], f[21], f[22], f[23]);
-      o.w = pack_e2m1x8(f[24], f[25], f[26], f[27], f[28], f[29], f[30], f[31]);
-      *reinterpret_cast<uint4*>(dst) = o;
-    } else {
-      uint4 o0, o1;
-      o0.x = pack_e4m3x4(f[0], f[1], f[2], f[3]);
-      o0.y = pack_e4m3x4(f[4], f[5], f[6], f[7]);
-      o0.z = pack_e4m3x4(f[8], f[9], f[10], f[11]);
-      o0.w = pack_e4m3x4(f[12], f[13], f[14], f[15]);
-      o1.x = pack_e4m3x4(f[16], f[17], f[18], f[19]);
-      o1.y = pack_e4m3x4(f[20], f[21], f[22], f[23]);
-      o1.z = pack_e4m3x4(f[24], f[25], f[26], f[27]);
-      o1.w = pack_e4m3x4(f[28], f[29], f[30], f[31]);
-      reinterpret_cast<uint4*>(dst)[0] = o0;
-      reinterpret_cast<uint4*>(dst)[1] = o1;
+    for (int hc = 0; hc < 2; ++hc) {
+      float f[32];
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        f[i] = hc ? bf_hi(w[i]) : bf_lo(w[i]);
+        amax = fmaxf(amax, fabsf(f[i]));
+      }
+      float inv;
+      const int X = block_exp<FMT>(amax, &inv);
+      const long long row = bh * D + c0 + hc;
+      scales[row * (Np / 32) + kb] = (uint8_t)(X + 127);
+      uint8_t* dst = codes + row * (long long)(Np * BYTES / 32) + kb * BYTES;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) f[i] *= inv;
+      if (FMT == 0) {
+        uint4 o;
+        o.x = pack_e2m1x8(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]);
+        o.y = pack_e2m1x8(f[8], f[9], f[10], f[11], f[12], f[13], f[14], f[15]);
+        o.z = pack_e2m1x8(f[16], f[17], f[18], f[19], f[20], f[21], f[22], f[23]);
+        o.w = pack_e2m1x8(f[24], f[25], f[26], f[27], f[28], f[29], f[30], f[31]);
+        *reinterpret_cast<uint4*>(dst) = o;
+      } else {
+        uint4 o0, o1;
+        o0.x = pack_e4m3x4(f[0], f[1], f[2], f[3]);
+        o0.y = pack_e4m3x4(f[4], f[5], f[6], f[7]);
+        o0.z = pack_e4m3x4(f[8], f[9], f[10], f[11]);
+        o0.w = pack_e4m3x4(f[12], f[13], f[14], f[15]);
+        o1.x = pack_e4m3x4(f[16], f[17], f[18], f[19]);
+        o1.y = pack_e4m3x4(f[20], f[21], f[22], f[23]);
+        o1.z = pack_e4m3x4(f[24], f[25], f[26], f[27]);
+        o1.w = pack_e4m3x4(f[28], f[29], f[30], f[31]);
+        reinterpret_cast<uint4*>(dst)[0] = o0;
+        reinterpret_cast<uint4*>(dst)[1] = o1;
+      }
     }
   }
 }
 
+// one warp per (b,h, 32-token block); nwarps = BH * Np / 32
 template <int FMT, int D>
-__global__ void __launch_bounds__(256) quant_cols_kernel(const __nv_bfloat16* __restrict__ x,
-                                                          int N, int Np,
-                                                          uint8_t* __restrict__ codes,
+__global__ void __launch_bounds__(256) quant_cols_kernel(const __nv_bfloat16* __restrict__ x, int N, int Np,
+                                                          long long nwarps, uint8_t* __restrict__ codes,
                                                           uint8_t* __restrict__ scales) {
-  __shared__ __align__(16) __nv_bfloat16 tile[128 * D];
-  quant_col_tile<FMT, D>(x, tile, N, Np, blockIdx.x * 128, blockIdx.y, codes, scales);
+  const long long wg = blockIdx.x * 8LL + threadIdx.x / 32;
+  if (wg >= nwarps) return;
+  const int nkb = Np / 32;
+  quant_col_block_warp<FMT, D>(x, wg / nkb, (int)(wg % nkb), N, Np, codes, scales, threadIdx.x % 32);
 }
 
 // Q and K (blocks along d) and V (blocks along N) in one grid.  CTA i is a V
-// tile when i is a multiple of `period` (the first nv of them), else a CTA of
-// 512 row blocks of Q, then of K: the transposes of V are spread among the row
-// streams instead of running after them.
+// CTA (eight 32-token blocks) when i is a multiple of `period` (the first nv
+// of them), else a CTA of 512 row blocks of Q, then of K: the V blocks are
+// spread among the row streams instead of running after them.
 template <int D>
 __global__ void __launch_bounds__(256) quant_qkv_kernel(const QkvParams p) {
-  __shared__ __align__(16) __nv_bfloat16 tile[128 * D];
   const long long i = blockIdx.x;
   const long long P = p.period;
   if (i % P == 0 && i / P < p.nv) {
-    const long long vt = i / P;
-    const int ntn = p.Np / 128;
-    quant_col_tile<0, D>(static_cast<const __nv_bfloat16*>(p.v), tile, p.N, p.Np, (int)(vt % ntn) * 128, vt / ntn, p.vc, p.vs);
+    // a V CTA: 8 warps, each one 32-token block of one (b, kv head)
+    const long long wg = (i / P) * 8 + threadIdx.x / 32;
+    const int nkb = p.Np / 32;
+    if (wg < p.nvw)
+      quant_col_block_warp<0, D>(static_cast<const __nv_bfloat16*>(p.v), wg / nkb, (int)(wg % nkb), p.N, p.Np,
+                                 p.vc, p.vs, threadIdx.x % 32);
     return;
   }
   const long long before = (i + P - 1) / P;
@@ -322,7 +330,8 @@ cudaError_t launch_quantize_qkv(const void* q, const void* k, const void* v, lon
   p.nbk = BHkv * N * (d / 32);
   p.nq_cta = (p.nbq + 511) / 512;
   p.nk_cta = (p.nbk + 511) / 512;
-  p.nv = (long long)(p.Np / 128) * BHkv;
+  p.nvw = (long long)(p.Np / 32) * BHkv;     // 32-token V blocks, one warp each
+  p.nv = (p.nvw + 7) / 8;                    // V CTAs of 8 warps
   const long long total = p.nv + p.nq_cta + p.nk_cta;
   p.period = total / p.nv;
   if (total > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -360,15 +369,16 @@ cudaError_t launch_quantize(const void* x, long long rows, int d, int N, long lo
       quant_rows_kernel<1><<<grid, 256, 0, st>>>((const uint4*)x, nblocks, (uint8_t*)codes,
                                                  (uint8_t*)scales);
   } else {
-    int Np = padded_n(N);
-    dim3 grid(Np / 128, (unsigned)BH);
+    const int Np = padded_n(N);
+    const long long nwarps = BH * (Np / 32);
+    const unsigned grid = (unsigned)((nwarps + 7) / 8);
     const __nv_bfloat16* xb = (const __nv_bfloat16*)x;
     if (d == 128) {
-      if (fmt == 0) quant_cols_kernel<0, 128><<<grid, 256, 0, st>>>(xb, N, Np, (uint8_t*)codes, (uint8_t*)scales);
-      else quant_cols_kernel<1, 128><<<grid, 256, 0, st>>>(xb, N, Np, (uint8_t*)codes, (uint8_t*)scales);
+      if (fmt == 0) quant_cols_kernel<0, 128><<<grid, 256, 0, st>>>(xb, N, Np, nwarps, (uint8_t*)codes, (uint8_t*)scales);
+      else quant_cols_kernel<1, 128><<<grid, 256, 0, st>>>(xb, N, Np, nwarps, (uint8_t*)codes, (uint8_t*)scales);
     } else {
-      if (fmt == 0) quant_cols_kernel<0, 64><<<grid, 256, 0, st>>>(xb, N, Np, (uint8_t*)codes, (uint8_t*)scales);
-      else quant_cols_kernel<1, 64><<<grid, 256, 0, st>>>(xb, N, Np, (uint8_t*)codes, (uint8_t*)scales);
+      if (fmt == 0) quant_cols_kernel<0, 64><<<grid, 256, 0, st>>>(xb, N, Np, nwarps, (uint8_t*)codes, (uint8_t*)scales);
+      else quant_cols_kernel<1, 64><<<grid, 256, 0, st>>>(xb, N, Np, nwarps, (uint8_t*)codes, (uint8_t*)scales);
     }
   }
   return cudaGetLastError();
