@@ -122,10 +122,11 @@ FA4FP4_API fa4fp4_status fa4fp4_fwd(const void* q_codes, const void* q_scales, c
  * Methodology 1: MXFP4 Q, K, V and the Direct-P forward), with the same
  * results as those two calls on the same data.  The pages have no
  * counterpart; this is the library's end-to-end entry point.  The work is cut
- * into chunks of (batch element, range of kv heads) with their query heads;
- * each chunk's inputs are copied in on an internal stream, quantized and
- * attended on `stream`, and copied out on a second internal stream, two
- * chunks' staging buffers in flight, so that the copies overlap the compute.
+ * into chunks of consecutive (batch element, kv head) units with their query
+ * heads, the last chunk a single unit; each chunk's inputs are copied in on
+ * an internal stream, quantized and attended alternately on `stream` and a
+ * second internal stream, and copied out on a third, two chunks' staging
+ * buffers in flight, so that the copies overlap the compute.
  * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for
  * the copies to overlap; q, k, v, o must be 16-byte aligned and lse 4-byte
  * aligned.  `workspace` is DEVICE memory of at least
@@ -134,7 +135,7 @@ FA4FP4_API fa4fp4_status fa4fp4_fwd(const void* q_codes, const void* q_scales, c
  * flight at the same time need their own workspaces.  The call is
  * asynchronous on `stream`: later work on `stream` sees o and lse in host
  * memory, and the call starts after earlier work on `stream`.  The first call
- * on a device creates two streams and seven events on it, kept until the
+ * on a device creates three streams and seven events on it, kept until the
  * process exits.  Other errors as fa4fp4_fwd's; all checks are made before
  * anything is enqueued, and a CUDA failure while enqueuing returns
  * FA4FP4_ERR_CUDA with the chunks before it already enqueued. */

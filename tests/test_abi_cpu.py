@@ -168,10 +168,10 @@ def test_fwd_host_validation_and_workspace(lib):
     OK, INVALID, UNSUP, ALIGN, WS = 0, 1, 2, 3, 6
     fh = lib.fa4fp4_fwd_host
     big = 1 << 40
-    # B4 Hq16 Hkv16 N4096 d128: two chunks of 8 heads per batch element; staging
-    # for two chunks of bf16 Q, K, V (8.4 MB each), two of O (f32) and LSE, and
-    # one chunk of MXFP4 Q, K, V^T codes and scales
-    want = 2 * 3 * 8 * 4096 * 128 * 2 + 2 * (8 * 4096 * 128 * 4 + 8 * 4096 * 4) + 3 * (8 * 4096 * 64 + 8 * 4096 * 4)
+    # B4 Hq16 Hkv16 N4096 d128: chunks of 8 (batch, kv head) units; staging for
+    # two chunks of bf16 Q, K, V (8.4 MB each), of O (f32) and LSE, and of MXFP4
+    # Q, K, V^T codes and scales
+    want = 2 * 3 * 8 * 4096 * 128 * 2 + 2 * (8 * 4096 * 128 * 4 + 8 * 4096 * 4) + 2 * 3 * (8 * 4096 * 64 + 8 * 4096 * 4)
     assert lib.fa4fp4_fwd_host_workspace_bytes(4, 16, 16, 4096, 128) == want
     assert lib.fa4fp4_fwd_host_workspace_bytes(1, 24, 24, 32760, 128) > 0
     assert lib.fa4fp4_fwd_host_workspace_bytes(1, 4, 3, 300, 128) == 0

@@ -3,9 +3,10 @@ path it chains (fa4fp4_quantize_qkv + fa4fp4_fwd) on the same data: the
 outputs must be bit-identical, whatever the chunking.  One case is also
 compared with the oracle (rel-L2 <= 1e-3, LSE to 1e-3 absolute).
 
-The shapes give 3, 4 and 6 chunks, so both staging sets are reused; two calls
-in a row share one workspace; pageable host tensors work too (their copies do
-not overlap)."""
+The shapes give 3, 4, 5 and 7 chunks, so both staging sets and both compute
+streams are reused, and one shape has chunks that cross a batch boundary;
+two calls in a row share one workspace; pageable host tensors work too (their
+copies do not overlap)."""
 import numpy as np
 import pytest
 import torch
@@ -37,6 +38,7 @@ def host_path(fa, q, k, v, causal, out_dtype, with_lse=True, pin=True, workspace
     (Workload("host_b2_hq8_hkv2_n300", 2, 8, 2, 300, 128, causal=True), 0, True),
     (Workload("host_b1_hq6_hkv3_n257_d64", 1, 6, 3, 257, 64), 1, False),
     (Workload("host_b3_h4_n130", 3, 4, 4, 130, 128), 0, True),
+    (Workload("host_b3_hq6_hkv3_n100_d64", 3, 6, 3, 100, 64, causal=True), 1, True),
 ])
 def test_matches_device_path(w, out_dtype, with_lse):
     fa = require_gpu()
