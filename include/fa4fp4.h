@@ -222,7 +222,10 @@ FA4FP4_API size_t fa4fp4_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int 
  *   v8r: MXFP8 V blocked along d ([B][Hkv][N][d]);
  *   o: forward output [B][Hq][N][d] (f32 or bf16 per o_dtype);
  *   dout: upstream gradient, bf16 [B][Hq][N][d];  lse: f32 [B][Hq][N].
- * Computes P = 2^(fmaf(s, c, -fl32(lse*log2 e))), D = rowsum(dO*O), the MXFP8
+ * Computes P = 2^x with x = fl32(s' c), s' = S + fl32(-fl32(lse*log2 e) / c)
+ * accumulated by the tensor core (S the FP4 product, c = scale*log2 e; within
+ * a few units in the last place of fmaf(S, c, -fl32(lse*log2 e))),
+ * D = rowsum(dO*O), the MXFP8
  * views of dO (blocks along d and blocks of 32 queries), dP = dO V^T, dS =
  * P*(dP-D), and, with P and dS quantized to MXFP8 (P and dS in blocks of 32
  * queries for dV/dK, dS in blocks of 32 keys for dQ; P's blocks take the
@@ -231,7 +234,8 @@ FA4FP4_API size_t fa4fp4_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int 
  * summed over the query heads of each kv head.  dq [B][Hq][N][d], dk/dv
  * [B][Hkv][N][d], all f32, fully overwritten.  `workspace` must hold
  * fa4fp4_bwd_workspace_bytes(...) bytes (FA4FP4_ERR_WORKSPACE otherwise); it
- * receives the MXFP8 views of dO and D and must not be shared with another
+ * receives the MXFP8 views of dO and, per query row, -fl32(lse*log2 e) / c and
+ * -D as bf16 parts (16 bytes), and must not be shared with another
  * call in flight.  d = 64 or 128. */
 FA4FP4_API fa4fp4_status fa4fp4_bwd(const void* q4_codes, const void* q4_scales, const void* k4_codes,
                          const void* k4_scales, const void* q8c_codes, const void* q8c_scales,

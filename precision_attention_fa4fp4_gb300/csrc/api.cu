@@ -291,9 +291,10 @@ size_t fa4fp4_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
   const size_t rows = (size_t)B * Hq * N;
   const size_t Np = (size_t)padded_n(N);
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  // dO row view (codes + scales), dO column view (codes + scales), D
+  // dO row view (codes + scales), dO column view (codes + scales), 16 bytes
+  // per row for the initial values of S^T and dP^T
   return up(rows * d) + up(rows * d / 32) + up((size_t)B * Hq * d * Np) +
-         up((size_t)B * Hq * d * Np / 32) + up(rows * sizeof(float));
+         up((size_t)B * Hq * d * Np / 32) + up(rows * 16);
 }
 
 fa4fp4_status fa4fp4_bwd(const void* q4c, const void* q4s, const void* k4c, const void* k4s,
@@ -323,12 +324,16 @@ fa4fp4_status fa4fp4_bwd(const void* q4c, const void* q4s, const void* k4c, cons
   uint8_t* do_r_s = w;         w += up(rows * d / 32);
   uint8_t* do_c = w;           w += up((size_t)B * Hq * d * Np);
   uint8_t* do_c_s = w;         w += up((size_t)B * Hq * d * Np / 32);
-  float* Dvec = reinterpret_cast<float*>(w);
+  uint8_t* fold = w;
+  const float scale = default_scale(softmax_scale, d);
+  const float c = (float)((double)scale * 1.4426950408889634);
+  const float l2e = (float)1.4426950408889634;
 
   BwdPrepParams pp;
   pp.o = o; pp.dout = dout; pp.o_bf16 = o_dtype == FA4FP4_OUT_BF16;
   pp.B = B; pp.Hq = Hq; pp.N = N; pp.d = d; pp.Np = Np;
-  pp.do_r = do_r; pp.do_r_s = do_r_s; pp.do_c = do_c; pp.do_c_s = do_c_s; pp.Dvec = Dvec; pp.dq = dq;
+  pp.do_r = do_r; pp.do_r_s = do_r_s; pp.do_c = do_c; pp.do_c_s = do_c_s; pp.dq = dq;
+  pp.lse = lse; pp.c = c; pp.l2e = l2e; pp.fold = reinterpret_cast<uint4*>(fold);
   cudaError_t e = launch_bwd_prep(pp, st);
   if (e != cudaSuccess) return FA4FP4_ERR_CUDA;
 
@@ -347,7 +352,8 @@ fa4fp4_status fa4fp4_bwd(const void* q4c, const void* q4s, const void* k4c, cons
       !make_map(&p.tm_do_r, u8, 1, do_r, d, N, BHq, d, 64, sw8) ||
       !make_map(&p.tm_q8c, u8, 1, q8c, Np, d, BHq, 64, d, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&p.tm_do_c, u8, 1, do_c, Np, d, BHq, 64, d, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&p.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq, d, N, BHq, d, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
+      !make_map(&p.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq, d, N, BHq, d, 64, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map(&p.tm_fold, u8, 1, fold, 16, N, BHq, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
     return FA4FP4_ERR_CUDA;
   p.q4_s = static_cast<const uint8_t*>(q4s);
   p.k4_s = static_cast<const uint8_t*>(k4s);
@@ -356,16 +362,14 @@ fa4fp4_status fa4fp4_bwd(const void* q4c, const void* q4s, const void* k4c, cons
   p.v8r_s = static_cast<const uint8_t*>(v8s);
   p.do_r_s = do_r_s;
   p.do_c_s = do_c_s;
-  p.lse = lse;
-  p.Dvec = Dvec;
   p.dq = dq; p.dk = dk; p.dv = dv;
   p.err = err_word();
   if (!p.err) return FA4FP4_ERR_CUDA;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.Np = Np;
   p.causal = causal ? 1 : 0;
-  p.scale = default_scale(softmax_scale, d);
-  p.c = (float)((double)p.scale * 1.4426950408889634);
-  p.l2e = (float)1.4426950408889634;
+  p.scale = scale;
+  p.c = c;
+  p.l2e = l2e;
   return launch_status(launch_bwd_main(p, st));
 }
 

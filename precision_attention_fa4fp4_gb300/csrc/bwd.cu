@@ -8,25 +8,40 @@
 // product contracts ("Gradient Formats"); the abstract adds FP8 gradient
 // operands for P, dS and dO.
 //
-// bwd_prep_kernel: D_i = sum_t dO_it O_it and zeroes dq (the main kernel
-//   adds into dq with bulk tensor reductions).  The MXFP8 views of dO come from the
+// bwd_prep_kernel: D_i = sum_t dO_it O_it, each query row's 16-byte row of
+//   initial values (-fl32(LSE_i log2 e) / c and -D_i, each as three bf16
+//   parts that sum to it exactly), and zeroes dq (the main kernel adds into dq
+//   with bulk tensor reductions).  The MXFP8 views of dO come from the
 //   quantize kernels.
 // bwd_kernel: one CTA per (batch, kv head, 128-key tile); loop over the query
 //   heads of the GQA group x 64-query tiles (causal: from the diagonal on).
-//   warp 0       producer (TMA + scale-chunk staging + LSE/D of the tile)
+//   warp 0       producer (TMA of the step's tiles and initial-value rows,
+//                scale-chunk staging)
 //   warp 1       TMEM owner + tcgen05 issuer:
-//                  S^T  = K4 Q4^T          kind::mxf4      M=128 keys, N=64
-//                  dP^T = V8r dOr^T        kind::mxf8f6f4  M=128 keys, N=64
+//                  S^T  = -LSE log2 e / c + K4 Q4^T
+//                                          kind::f16 (ones x initial-value
+//                                          rows, K = 16) then kind::mxf4,
+//                                          M=128 keys, N=64
+//                  dP^T = -D + V8r dOr^T   kind::f16 then kind::mxf8f6f4
 //                  dV  += Pq^T dOc         M=128 keys, N=d, K=64 queries
 //                  dK  += dSc^T Q8c        M=128 keys, N=d
 //                  dQ^T = K8c^T dSr        M=d, N=64 queries, K=128 keys
 //                                          (B operand MN-major)
-//   warps 2-9    one key row x 32 queries per thread: P = 2^(fmaf(s, c,
-//                -fl32(LSE log2 e))), dS = P (dP - D), quantized to MXFP8:
+//   warps 2-9    one key row x 32 queries per thread: P = 2^(c s'), s' the
+//                accumulator S - LSE log2 e / c, dS = P (dP - D) with dP - D
+//                read from its accumulator, quantized to MXFP8:
 //                P and dS in blocks of 32 queries (thread-local), dS in
 //                blocks of 32 keys (warp-wide max with redux.sync).
 //   warps 10-13  dQ^T from TMEM, times softmax_scale, added into dq.
 //   After the loop: dV and dK * softmax_scale written by warps 2-9.
+// Starting the accumulators at the per-query offsets (an MMA of a constant
+// ones operand with the step's initial-value rows) takes the LSE and D
+// operands off the P/dS warps (no per-query shared-memory loads, one multiply
+// per score instead of an FMA and a subtraction) and off the producer (the
+// rows arrive by TMA with the step's tiles).  The exponent is formed as
+// fl32(fl32(S + t) c) instead of fmaf(S, c, -fl32(LSE log2 e)): both round
+// once at the magnitude of S or of LSE log2 e / c, so they differ by a few
+// units in the last place of x.
 // d = 64 or 128 (template D).  Block-scaled MMAs have M = 128, so at d = 64
 // the A operand of dQ^T (K8c^T, d rows) is padded to 128 rows with zeros in
 // shared memory and the extra 64 TMEM lanes of dQ^T are not read.
@@ -42,7 +57,7 @@ namespace {
 
 constexpr int BK = 128;          // keys per CTA
 constexpr int BQ = 64;           // queries per step
-constexpr int NST = 3;           // input stages (Q4, dOr, Q8, dOc of a step)
+constexpr int NST = 3;           // input stages (Q4, dOr, Q8, dOc and initial-value rows of a step)
 constexpr int BWD_GROUP = 4;     // causal CTA order: kv heads per group
 constexpr int NTHREADS = 14 * 32;
 constexpr uint32_t TMEM_COLS = 512;
@@ -65,8 +80,11 @@ struct BL {   // shared-memory layout (bytes)
   static constexpr int SFC = DSR + 2 * BK * BQ;      // scale chunks, 512 B each
   // chunk ids: 0 K4, 1 V8, 2 K8, 3-4 P, 5-6 dSc, 7-8 dSr (by step parity),
   // 9 + 4 * stage + {0 Q4, 1 dOr, 2 Q8, 3 dOc}
-  static constexpr int VEC = SFC + (9 + 4 * NST) * 512;   // float lse2[NST][64], dvec[NST][64]
-  static constexpr int DQS = VEC + 2 * NST * BQ * 4;      // dQ tile [64 q][128 d] fp32
+  // [NST] x 64 query rows x 16 B: bf16 parts of -LSE log2 e / c and of -D
+  // (the B operand of the accumulator-initialising MMAs)
+  static constexpr int FOLD = SFC + (9 + 4 * NST) * 512;
+  static constexpr int ONES = FOLD + NST * BQ * 16;       // A operands: [rows 1,1,1,0..][0,0,0,1,1,1,0,0][zeros]
+  static constexpr int DQS = ONES + 384;                  // dQ tile [64 q][128 d] fp32
   static constexpr int OKS = DQS + BQ * D * 4;             // int [4]: dQ writers' status
   static constexpr int BAR = OKS + 16;
   static constexpr int NBAR = 1 + NST + NST + 1 + 1 + 2 + 1 + 1 + 1 + 1;
@@ -102,6 +120,29 @@ FA4_DEV uint4 load_chunk(const uint8_t* __restrict__ src, long long stride, int 
 FA4_DEV void stage_chunk(uint8_t* chunk, const uint8_t* src, long long stride, int nvalid,
                          int bpr, int lane) {
   *reinterpret_cast<uint4*>(chunk + lane * 16) = load_chunk(src, stride, nvalid, bpr, lane);
+}
+
+// One 16-byte row of the initialising MMAs' B operand: a and b each as three
+// bf16 parts, then two zeros.  Round-to-nearest splitting: each part takes
+// the next 8 significant bits of the remainder, and each remainder is exact in
+// FP32, so the three parts sum exactly to any float of magnitude >= 2^-110
+// (below that the last part loses bits to bf16 subnormals).
+FA4_DEV uint4 fold_row(float a, float b) {
+  uint16_t h[8];
+  const float v[2] = {a, b};
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    float r = v[j];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const __nv_bfloat16 t = __float2bfloat16_rn(r);
+      h[3 * j + k] = __bfloat16_as_ushort(t);
+      r -= __bfloat162float(t);
+    }
+  }
+  h[6] = h[7] = 0;
+  return make_uint4(h[0] | (uint32_t)h[1] << 16, h[2] | (uint32_t)h[3] << 16, h[4] | (uint32_t)h[5] << 16,
+                    h[6] | (uint32_t)h[7] << 16);
 }
 
 // 32 floats * inv -> 32 E4M3 codes as two uint4 (element 0 in byte 0)
@@ -157,8 +198,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + BL::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + BL::MISC + 4);
   uint8_t* sfc = smem + BL::SFC;
-  float* lse2 = reinterpret_cast<float*>(smem + BL::VEC);     // [2][64]
-  float* dvec = lse2 + NST * BQ;                               // [NST][64]
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // CTA order: groups of G (batch, kv head) pairs, key tile major inside a
@@ -200,10 +239,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(tmem_holder, TMEM_COLS);
-  if (D < 128 && warp >= 2) {
-    // zero rows d..127 of the K8c^T operand (the TMA fills rows 0..d-1)
-    uint4* z = reinterpret_cast<uint4*>(smem + BL::K8 + D * BK);
-    for (int i = threadIdx.x - 64; i < (128 - D) * BK / 16; i += NTHREADS - 64) z[i] = make_uint4(0, 0, 0, 0);
+  if (warp >= 2) {
+    if (D < 128) {
+      // zero rows d..127 of the K8c^T operand (the TMA fills rows 0..d-1)
+      uint4* z = reinterpret_cast<uint4*>(smem + BL::K8 + D * BK);
+      for (int i = threadIdx.x - 64; i < (128 - D) * BK / 16; i += NTHREADS - 64) z[i] = make_uint4(0, 0, 0, 0);
+    }
+    // the constant A operands of the initialising MMAs: one 8-row core matrix
+    // each (every row group reads it), bf16 ones in K columns 0-2 or 3-5,
+    // then a zero core matrix for K columns 8-15
+    const int i = threadIdx.x - 64;
+    if (i < 24) {
+      const uint32_t one = 0x3f80u;
+      const uint4 v = i < 8 ? make_uint4(one | one << 16, one, 0, 0)
+                            : (i < 16 ? make_uint4(0, one << 16, one | one << 16, 0) : make_uint4(0, 0, 0, 0));
+      reinterpret_cast<uint4*>(smem + BL::ONES)[i] = v;
+    }
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -238,35 +289,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
       const int nq_valid = min(BQ, p.N - q0);
       if (lane == 0) {
         uint8_t* sb = smem + BL::STG + st * BL::STAGE_BYTES;
-        mbar_arrive_expect_tx(&in_full[st], BL::STAGE_BYTES);
+        mbar_arrive_expect_tx(&in_full[st], BL::STAGE_BYTES + BQ * 16);
         tma_load_3d(sb + BL::Q4, &p.tm_q4, &in_full[st], 0, q0, bh);
         tma_load_3d(sb + BL::DOR, &p.tm_do_r, &in_full[st], 0, q0, bh);
         tma_load_3d(sb + BL::Q8, &p.tm_q8c, &in_full[st], q0, 0, bh);
         tma_load_3d(sb + BL::DOC, &p.tm_do_c, &in_full[st], q0, 0, bh);
+        tma_load_3d(smem + BL::FOLD + st * BQ * 16, &p.tm_fold, &in_full[st], 0, q0, bh);
       }
-      // scale chunks, LSE log2 e and D of the stage, while its tiles are in
-      // flight: every load is issued before the first shared-memory store
+      // scale chunks of the stage, while its tiles are in flight: every load
+      // is issued before the first shared-memory store
       uint8_t* sc = sfc + (9 + 4 * st) * 512;
       const uint4 c0 = load_chunk(p.q4_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, D / 32, lane);
       const uint4 c1 = load_chunk(p.do_r_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, D / 32, lane);
       const uint4 c2 = load_chunk(p.q8c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
       const uint4 c3 = load_chunk(p.do_c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
-      float l2[2], dd[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int q = q0 + lane + 32 * u;
-        l2[u] = q < p.N ? __ldg(p.lse + (long long)bh * p.N + q) * p.l2e : 0.f;
-        dd[u] = q < p.N ? __ldg(p.Dvec + (long long)bh * p.N + q) : 0.f;
-      }
       reinterpret_cast<uint4*>(sc)[lane] = c0;
       reinterpret_cast<uint4*>(sc + 512)[lane] = c1;
       reinterpret_cast<uint4*>(sc + 1024)[lane] = c2;
       reinterpret_cast<uint4*>(sc + 1536)[lane] = c3;
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        lse2[st * BQ + lane + 32 * u] = l2[u];
-        dvec[st * BQ + lane + 32 * u] = dd[u];
-      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&in_full[st]);
@@ -286,9 +326,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
     const uint32_t id_dp = idesc_bs(128, BQ, 0, 0, false, false, 0, 0);      // mxf8 e4m3
     const uint32_t id_acc = idesc_bs(128, D, 0, 0, false, false, 0, 0);   // N = d
     const uint32_t id_dq = idesc_bs(128, BQ, 0, 0, false, true, 0, 0);
+    const uint32_t id_fold = idesc_f16(128, BQ, true, false, false);      // bf16, K = 16
     const uint32_t s_k4 = smem_u32(smem + BL::K4), s_v8 = smem_u32(smem + BL::V8),
                    s_k8 = smem_u32(smem + BL::K8), s_pq = smem_u32(smem + BL::PQ),
-                   s_dsc = smem_u32(smem + BL::DSC), s_dsr = smem_u32(smem + BL::DSR);
+                   s_dsc = smem_u32(smem + BL::DSC), s_dsr = smem_u32(smem + BL::DSR),
+                   s_fold = smem_u32(smem + BL::FOLD), s_ones = smem_u32(smem + BL::ONES);
     bool ok = mbar_wait(fix_full, 0, abort_flag, p.err);
     tc_fence_after();
     if (ok && leader) {
@@ -311,19 +353,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
         tmem_cp_sf(tbase + SF_DOR + 4 * sp, sc + 512);
         tmem_cp_sf(tbase + SF_Q8 + 4 * sp, sc + 1024);
         tmem_cp_sf(tbase + SF_DOC + 4 * sp, sc + 1536);
+        // S^T starts at -LSE log2 e / c and dP^T at -D of each query column:
+        // ones (128 x 16, K columns 0-2 or 3-5) times the stage's bf16 parts
+        // (64 x 16; the descriptor's K offset 0 repeats columns 0-7 as 8-15,
+        // which meet the zero half of A)
+        const uint64_t fb = make_sdesc(s_fold + st * BQ * 16, 0, 128, SW_NONE);
+        mma_f16(tbase + COL_ST, make_sdesc(s_ones, 256, 0, SW_NONE), fb, id_fold, false);
+        mma_f16(tbase + COL_DPT, make_sdesc(s_ones + 128, 128, 0, SW_NONE), fb, id_fold, false);
 #pragma unroll
         for (int k = 0; k < D / 64; ++k) {     // K = d: K64 steps
           const uint32_t sf = ((uint32_t)(2 * k) << 29) | ((uint32_t)(2 * k) << 4);
           mma_mxf4(tbase + COL_ST, make_sdesc(s_k4 + 32 * k, 16, SBO4, SW4),
                    make_sdesc(sb + BL::Q4 + 32 * k, 16, SBO4, SW4), id_st | sf, tbase + SF_K4,
-                   tbase + SF_Q4 + 4 * sp, k > 0);
+                   tbase + SF_Q4 + 4 * sp, true);
         }
 #pragma unroll
         for (int k = 0; k < D / 32; ++k) {     // K = d: K32 steps
           const uint32_t sf = ((uint32_t)k << 29) | ((uint32_t)k << 4);
           mma_mxf8(tbase + COL_DPT, make_sdesc(s_v8 + 32 * k, 16, SBO8, SW8),
                    make_sdesc(sb + BL::DOR + 32 * k, 16, SBO8, SW8), id_dp | sf, tbase + SF_V8,
-                   tbase + SF_DOR + 4 * sp, k > 0);
+                   tbase + SF_DOR + 4 * sp, true);
         }
         mma_commit(s_full);
       }
@@ -413,50 +462,35 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(st_free);
-      // LSE log2 e and D of this thread's 32 queries, four at a time (16-byte
-      // aligned rows)
-      const float4* l4 = reinterpret_cast<const float4*>(lse2 + st * BQ + 32 * g);
-      const float4* d4 = reinterpret_cast<const float4*>(dvec + st * BQ + 32 * g);
       const int qbase = q0 + 32 * g;
       float pmax = 0.f, dsmax = 0.f;
       // every (key, query) of this warp's block in range and unmasked: the
       // same arithmetic without the per-element validity test
       const bool full = k0 + BK <= p.N && qbase + 32 <= p.N && (!p.causal || k0 + BK - 1 <= qbase);
+      // s holds S - LSE log2 e / c and dp holds dP - D (the accumulators
+      // started there)
       if (full) {
 #pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 la = l4[i4], da = d4[i4];
-          const float l2q[4] = {la.x, la.y, la.z, la.w}, dq4[4] = {da.x, da.y, da.z, da.w};
-#pragma unroll
-          for (int e = 0; e < 4; e += 2) {
-            const int i = 4 * i4 + e;
-            const float2 x = ffma2(make_float2(s[i], s[i + 1]), make_float2(c, c),
-                                   make_float2(-l2q[e], -l2q[e + 1]));
-            const float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            const float2 ds = fmul2(pv, fadd2(make_float2(dp[i], dp[i + 1]), make_float2(-dq4[e], -dq4[e + 1])));
-            s[i] = pv.x; s[i + 1] = pv.y;
-            dp[i] = ds.x; dp[i + 1] = ds.y;
-            pmax = fmax3(pmax, pv.x, pv.y);
-            dsmax = fmax3(dsmax, fabsf(ds.x), fabsf(ds.y));
-          }
+        for (int i = 0; i < 32; i += 2) {
+          const float2 x = fmul2(make_float2(s[i], s[i + 1]), make_float2(c, c));
+          const float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          const float2 ds = fmul2(pv, make_float2(dp[i], dp[i + 1]));
+          s[i] = pv.x; s[i + 1] = pv.y;
+          dp[i] = ds.x; dp[i + 1] = ds.y;
+          pmax = fmax3(pmax, pv.x, pv.y);
+          dsmax = fmax3(dsmax, fabsf(ds.x), fabsf(ds.y));
         }
       } else {
 #pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 la = l4[i4], da = d4[i4];
-          const float l2q[4] = {la.x, la.y, la.z, la.w}, dq4[4] = {da.x, da.y, da.z, da.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = 4 * i4 + e;
-            const int q = qbase + i;
-            const bool valid = key < p.N && q < p.N && (!p.causal || key <= q);
-            const float pv = valid ? ex2_approx(fmaf(s[i], c, -l2q[e])) : 0.f;
-            const float ds = pv * (dp[i] - dq4[e]);
-            s[i] = pv;
-            dp[i] = ds;
-            pmax = fmaxf(pmax, pv);
-            dsmax = fmaxf(dsmax, fabsf(ds));
-          }
+        for (int i = 0; i < 32; ++i) {
+          const int q = qbase + i;
+          const bool valid = key < p.N && q < p.N && (!p.causal || key <= q);
+          const float pv = valid ? ex2_approx(s[i] * c) : 0.f;
+          const float ds = pv * dp[i];
+          s[i] = pv;
+          dp[i] = ds;
+          pmax = fmaxf(pmax, pv);
+          dsmax = fmaxf(dsmax, fabsf(ds));
         }
       }
       // P and dS in blocks of 32 queries (this thread's columns); P under the
@@ -598,11 +632,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
   if (warp == 1) tmem_dealloc(tbase, TMEM_COLS);
 }
 
-// D_i = sum_t dO_it * O_it (one warp per row) and dq = 0.
+// D_i = sum_t dO_it * O_it (one warp per row), the row's initial values
+// -fl32(LSE_i log2 e) / c and -D_i as bf16 parts, and dq = 0.
 template <int D, bool O_BF16>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const void* __restrict__ o,
                                                         const __nv_bfloat16* __restrict__ dout,
-                                                        long long rows, float* __restrict__ Dvec,
+                                                        const float* __restrict__ lse, float c, float l2e,
+                                                        long long rows, uint4* __restrict__ fold,
                                                         float* __restrict__ dq) {
   const int lane = threadIdx.x % 32;
   const long long wpb = blockDim.x / 32;
@@ -651,7 +687,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const void* __restrict__ 
     for (int u = 0; u < E; ++u) acc += dof[u] * of[u];
 #pragma unroll
     for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) Dvec[row] = acc;
+    if (lane == 0) fold[row] = fold_row(-(lse[row] * l2e) / c, -acc);
     if constexpr (E == 4) *reinterpret_cast<float4*>(dq + base) = make_float4(0.f, 0.f, 0.f, 0.f);
     else *reinterpret_cast<float2*>(dq + base) = make_float2(0.f, 0.f);
   }
@@ -668,11 +704,11 @@ cudaError_t launch_bwd_prep(const BwdPrepParams& p, cudaStream_t st) {
   int grid = (int)(blocks < 152 * 16 ? blocks : 152 * 16);
   const __nv_bfloat16* dout = (const __nv_bfloat16*)p.dout;
   if (p.d == 128) {
-    if (p.o_bf16) bwd_prep_kernel<128, true><<<grid, 256, 0, st>>>(p.o, dout, rows, p.Dvec, p.dq);
-    else bwd_prep_kernel<128, false><<<grid, 256, 0, st>>>(p.o, dout, rows, p.Dvec, p.dq);
+    if (p.o_bf16) bwd_prep_kernel<128, true><<<grid, 256, 0, st>>>(p.o, dout, p.lse, p.c, p.l2e, rows, p.fold, p.dq);
+    else bwd_prep_kernel<128, false><<<grid, 256, 0, st>>>(p.o, dout, p.lse, p.c, p.l2e, rows, p.fold, p.dq);
   } else {
-    if (p.o_bf16) bwd_prep_kernel<64, true><<<grid, 256, 0, st>>>(p.o, dout, rows, p.Dvec, p.dq);
-    else bwd_prep_kernel<64, false><<<grid, 256, 0, st>>>(p.o, dout, rows, p.Dvec, p.dq);
+    if (p.o_bf16) bwd_prep_kernel<64, true><<<grid, 256, 0, st>>>(p.o, dout, p.lse, p.c, p.l2e, rows, p.fold, p.dq);
+    else bwd_prep_kernel<64, false><<<grid, 256, 0, st>>>(p.o, dout, p.lse, p.c, p.l2e, rows, p.fold, p.dq);
   }
   return cudaGetLastError();
 }

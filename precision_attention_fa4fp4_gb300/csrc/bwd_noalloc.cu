@@ -4,7 +4,8 @@
 // device allocation, runtimes that forbid allocation after start-up, or code
 // whose device memory is budgeted once up front.  For them this file provides
 // fa4fp4_bwd_noalloc, which runs the same backward as
-// fa4fp4_bwd but takes its scratch (the MXFP8 views of dO and the row sums D)
+// fa4fp4_bwd but takes its scratch (the MXFP8 views of dO and the per-row
+// initial values of S^T and dP^T)
 // from a fixed array in device memory instead of a caller workspace.
 //
 // The array is a file-scope __device__ variable of FA4FP4_BWD_NOALLOC_SCRATCH_BYTES

@@ -79,9 +79,8 @@ struct BwdParams {
   CUtensorMap tm_v8r;                // MXFP8 row view of V [bh][N][d]
   CUtensorMap tm_do_r, tm_do_c;      // MXFP8 views of dO (workspace)
   CUtensorMap tm_dq;                 // dq fp32 [bh][N][d], for bulk reductions
+  CUtensorMap tm_fold;               // [bh][N] x 16 B: bf16 parts of -LSE log2 e / c and -D (workspace)
   const uint8_t *q4_s, *k4_s, *q8c_s, *k8c_s, *v8r_s, *do_r_s, *do_c_s;
-  const float* lse;
-  const float* Dvec;                 // rowsum(dO*O), workspace
   float *dq, *dk, *dv;
   unsigned* err;
   int B, Hq, Hkv, N, d, Np, causal;
@@ -93,7 +92,9 @@ struct BwdPrepParams {
   int o_bf16;
   int B, Hq, N, d, Np;
   uint8_t *do_r, *do_r_s, *do_c, *do_c_s;
-  float* Dvec;
+  const float* lse;
+  float c, l2e;
+  uint4* fold;                       // per row: bf16 parts of -LSE log2 e / c and of -D
   float* dq;
 };
 cudaError_t launch_bwd_prep(const BwdPrepParams& p, cudaStream_t st);
