@@ -352,7 +352,7 @@ fa4fp4_status fa4fp4_bwd(const void* q4c, const void* q4s, const void* k4c, cons
       !make_map(&p.tm_do_r, u8, 1, do_r, d, N, BHq, d, 64, sw8) ||
       !make_map(&p.tm_q8c, u8, 1, q8c, Np, d, BHq, 64, d, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&p.tm_do_c, u8, 1, do_c, Np, d, BHq, 64, d, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&p.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq, d, N, BHq, d, 64, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map(&p.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq, d, N, BHq, d, 32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_map(&p.tm_fold, u8, 1, fold, 16, N, BHq, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
     return FA4FP4_ERR_CUDA;
   p.q4_s = static_cast<const uint8_t*>(q4s);

@@ -32,7 +32,10 @@
 //                read from its accumulator, quantized to MXFP8:
 //                P and dS in blocks of 32 queries (thread-local), dS in
 //                blocks of 32 keys (warp-wide max with redux.sync).
-//   warps 10-13  dQ^T from TMEM, times softmax_scale, added into dq.
+//   warps 10-13  dQ^T from TMEM, times softmax_scale, added into dq in two
+//                halves of 32 queries, each staged in shared memory and added
+//                by its own bulk tensor reduction (staging one half overlaps
+//                the reduction still reading the other).
 //   After the loop: dV and dK * softmax_scale written by warps 2-9.
 // Starting the accumulators at the per-query offsets (an MMA of a constant
 // ones operand with the step's initial-value rows) takes the LSE and D
@@ -587,6 +590,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
     float* stage = reinterpret_cast<float*>(smem + BL::DQS);
     int* okw = reinterpret_cast<int*>(smem + BL::OKS);
     const bool issuer = warp == 10 && lane == 0;
+    bool prev_b = false;
     for (int t = 0; t < nsteps; ++t) {
       const int h = hk * group + t / per_head;
       const int q0 = (i0 + t % per_head) * BQ;
@@ -605,23 +609,40 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
       }
       __syncwarp();
       if (lane == 0 && wok) mbar_arrive(dq_free);
-      // the previous step's reduction has read the staging tile
-      if (issuer) bulk_wait_read0();
+      // the staging tile is two halves of 32 queries, each added into dq by
+      // its own bulk reduction: half A of this step is written once the
+      // previous step's half A has been read (its half B may still be read),
+      // and half B once the previous half B has been read (a step whose
+      // second half lies past N issues no reduction for it)
+      if (issuer) {
+        if (prev_b) bulk_wait_read1();
+        else bulk_wait_read0();
+      }
       const bool all_ok = __all_sync(0xffffffffu, wok);
       if (lane == 0) okw[warp - 10] = all_ok ? 1 : 0;
       named_bar(1, 128);
       if (!(okw[0] & okw[1] & okw[2] & okw[3])) break;
       if (drow < D) {     // TMEM lanes d..127 hold the zero rows of the padded operand
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          stage[i * D + drow] = __uint_as_float(v0[i]) * p.scale;
-          stage[(32 + i) * D + drow] = __uint_as_float(v1[i]) * p.scale;
-        }
+        for (int i = 0; i < 32; ++i) stage[i * D + drow] = __uint_as_float(v0[i]) * p.scale;
       }
       fence_proxy_async_smem();
       named_bar(1, 128);
       if (issuer) {
         tma_reduce_add_3d(&p.tm_dq, stage, 0, q0, b * p.Hq + h);
+        bulk_commit();
+        bulk_wait_read1();
+      }
+      named_bar(1, 128);
+      if (drow < D) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) stage[(32 + i) * D + drow] = __uint_as_float(v1[i]) * p.scale;
+      }
+      fence_proxy_async_smem();
+      named_bar(1, 128);
+      prev_b = q0 + 32 < p.N;
+      if (issuer && prev_b) {
+        tma_reduce_add_3d(&p.tm_dq, stage + 32 * D, 0, q0 + 32, b * p.Hq + h);
         bulk_commit();
       }
     }
