@@ -267,8 +267,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // The tile loads go first; the scale chunks (plain loads by the warp)
-    // are fetched while they are in flight.
+    // The key tile's loads go first; its scale chunks (plain loads by the
+    // warp) are fetched while they are in flight.
     const int nk_valid = min(BK, p.N - k0);
     if (lane == 0) {
       mbar_arrive_expect_tx(fix_full, BK * D / 2 + BK * D + D * BK);
@@ -283,13 +283,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
     __syncwarp();
     if (lane == 0) mbar_arrive(fix_full);
     int issued = 0;
+    // The scale-chunk words of a step are loaded into registers before the
+    // producer waits for that step's stage to be released, so their latency
+    // overlaps the wait; the tile loads are issued as soon as it is free.
+    uint4 c0, c1, c2, c3;
+    auto load_chunks = [&](int t) {
+      const int bh = b * p.Hq + hk * group + t / per_head;
+      const int q0 = (i0 + t % per_head) * BQ;
+      const int nq_valid = min(BQ, p.N - q0);
+      c0 = load_chunk(p.q4_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, D / 32, lane);
+      c1 = load_chunk(p.do_r_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, D / 32, lane);
+      c2 = load_chunk(p.q8c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
+      c3 = load_chunk(p.do_c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
+    };
+    if (nsteps > 0) load_chunks(0);
     for (int t = 0; t < nsteps; ++t) {
       const int st = t % NST;
       const int h = hk * group + t / per_head;
       const int q0 = (i0 + t % per_head) * BQ;
       const int bh = b * p.Hq + h;
       if (t >= NST && !mbar_wait(&in_empty[st], ((t / NST) - 1) & 1, abort_flag, p.err)) break;
-      const int nq_valid = min(BQ, p.N - q0);
       if (lane == 0) {
         uint8_t* sb = smem + BL::STG + st * BL::STAGE_BYTES;
         mbar_arrive_expect_tx(&in_full[st], BL::STAGE_BYTES + BQ * 16);
@@ -299,13 +312,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
         tma_load_3d(sb + BL::DOC, &p.tm_do_c, &in_full[st], q0, 0, bh);
         tma_load_3d(smem + BL::FOLD + st * BQ * 16, &p.tm_fold, &in_full[st], 0, q0, bh);
       }
-      // scale chunks of the stage, while its tiles are in flight: every load
-      // is issued before the first shared-memory store
       uint8_t* sc = sfc + (9 + 4 * st) * 512;
-      const uint4 c0 = load_chunk(p.q4_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, D / 32, lane);
-      const uint4 c1 = load_chunk(p.do_r_s + ((long long)bh * p.N + q0) * (D / 32), D / 32, nq_valid, D / 32, lane);
-      const uint4 c2 = load_chunk(p.q8c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
-      const uint4 c3 = load_chunk(p.do_c_s + (long long)bh * D * (p.Np / 32) + q0 / 32, p.Np / 32, D, 2, lane);
       reinterpret_cast<uint4*>(sc)[lane] = c0;
       reinterpret_cast<uint4*>(sc + 512)[lane] = c1;
       reinterpret_cast<uint4*>(sc + 1024)[lane] = c2;
@@ -314,6 +321,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_kernel(const __grid_constant_
       __syncwarp();
       if (lane == 0) mbar_arrive(&in_full[st]);
       issued = t + 1;
+      if (t + 1 < nsteps) load_chunks(t + 1);
     }
     if (*abort_flag && lane == 0) {
       volatile int no_abort = 0;
