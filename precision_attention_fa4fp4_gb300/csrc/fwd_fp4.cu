@@ -94,17 +94,25 @@ FA4_DEV uint32_t directp_code(float x, const float (&T)[7]) {
 }
 
 // Codes of 32 consecutive scores, packed 8 per word (element e of word w in
-// nibble e).  Native-exponential route made exact: with x = fmaf(s, c, -mc)
-// (the method's offset) and e = ex2(x), the codes of 6e(1-eps) and 6e(1+eps)
-// bracket the code of the exact 6*2^x, because rounding to E2M1 is monotone
-// and eps = 2^-18 exceeds the error of ex2 plus the two products.  Where the
-// bracket is one code wide that code is the exact one; the lanes where it is
-// not (scores within eps of an E2M1 midpoint) redo their scores with the
-// threshold count.  Returns the packed codes in pw.
-constexpr float K_LO = 6.0f * (1.0f - 0x1p-18f), K_HI = 6.0f * (1.0f + 0x1p-18f);
+// nibble e).  Native-exponential route made exact.  The method's offset is
+// x = fmaf(s, c, -mc); the lane instead forms x' = fmaf(s, c, klo) with
+// klo = (log2 6 - eps) - mc, so ylo = ex2(x') is 6 2^x 2^-eps up to the
+// rounding of klo and x' and the error of ex2, and yhi = ylo R.  With
+// eps = 2^-19 + 2u and R = 1 + 2^-18 + 3u (u = ulp(mc)), ylo < 6 2^x < yhi:
+// where 6 2^x is near an E2M1 midpoint (|x| < 8) those roundings move x' by
+// at most 2^-20 + u, and ex2 is within 2^-22 relative.  Rounding to E2M1 is
+// monotone, so where the codes of ylo and yhi agree that code is the exact
+// one; the lanes where they do not (scores within about 2^-18 of a midpoint)
+// redo their scores with the threshold count.  Folding the factor 6 and the
+// lower bracket into x' leaves one product per score (yhi).  Returns the
+// packed codes in pw.
+constexpr float LOG2_6 = 0x1.4ae00ep+1f;   // fl32(log2 6), within 2^-23.2 of it
 
 FA4_DEV void directp_codes32(const float (&s)[32], float c, float mc, const float (&T)[7],
                              uint32_t (&pw)[4]) {
+  const float u = __uint_as_float(__float_as_uint(mc) & 0x7f800000u) * 0x1p-23f;   // ulp(mc), normal mc
+  const float klo = (LOG2_6 - fmaf(2.f, u, 0x1p-19f)) - mc;
+  const float R = 1.f + fmaf(3.f, u, 0x1p-18f);
   bool ambiguous = false;
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
@@ -112,10 +120,9 @@ FA4_DEV void directp_codes32(const float (&s)[32], float c, float mc, const floa
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
       const float2 x = ffma2(make_float2(s[8 * w + e], s[8 * w + e + 1]), make_float2(c, c),
-                             make_float2(-mc, -mc));
-      const float2 ex = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-      const float2 a = fmul2(ex, make_float2(K_LO, K_LO));
-      const float2 b = fmul2(ex, make_float2(K_HI, K_HI));
+                             make_float2(klo, klo));
+      const float2 a = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+      const float2 b = fmul2(a, make_float2(R, R));
       ylo[e] = a.x; ylo[e + 1] = a.y;
       yhi[e] = b.x; yhi[e + 1] = b.y;
     }

@@ -38,9 +38,11 @@ def test_random_scores_and_maxima():
 
 
 def test_native_exponential_route_is_exact():
-    """The forward's route (ex2 + bracketed RNE to E2M1, threshold count where
-    the bracket is ambiguous) must equal the exact threshold map for every
-    FP32 offset in [-6, -2^-8] (the classifier depends on x alone)."""
+    """The forward's route (ex2 of fmaf(s, c, log2 6 - eps - mc) + bracketed
+    RNE to E2M1, threshold count where the bracket is ambiguous) must equal
+    the exact threshold map for every FP32 offset in [-6, -2^-8] (with m = 0
+    and c = 1 the offset is the score itself; the bracket's width depends on
+    mc, which the random tests below vary)."""
     fa = require_gpu()
     neg = np.arange(np.float32(2.0 ** -8).view(np.int32), np.float32(6.0).view(np.int32) + 1, dtype=np.int32)
     x = np.concatenate([-(neg.view(np.float32)),
@@ -51,11 +53,15 @@ def test_native_exponential_route_is_exact():
     assert bad.size == 0, f"{bad.size} codes differ, e.g. x={x[bad[:5]]} gpu={got[bad[:5]]} oracle={want[bad[:5]]}"
 
 
-def test_native_route_random_scores_and_maxima():
+@pytest.mark.parametrize("m_std", [3.0, 30.0, 300.0])
+def test_native_route_random_scores_and_maxima(m_std):
+    """Scores below a random maximum m: |m c| small (the narrowest bracket),
+    moderate and large (the bracket widens with the unit in the last place of
+    m c, which the rounding of klo adds to the offset)."""
     fa = require_gpu()
     rng = np.random.default_rng(1)
     for _ in range(10):
-        m = np.float32(rng.standard_normal() * 300)
+        m = np.float32(rng.standard_normal() * m_std)
         c = np.float32(rng.uniform(0.05, 0.3))
         s = (m - np.abs(rng.standard_normal(200003)) * 40).astype(np.float32)
         got = fa.directp_codes(torch.from_numpy(s).cuda(), float(m), float(c), native_exp=True).cpu().numpy()
