@@ -71,7 +71,6 @@ struct Layout {
   static constexpr int NBAR = 1 + 4 * STAGES + 2 + 2 + 2 + 2 + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int BYTES = OFF_MISC + 64 + 1024;    // + alignment slack
-  // TMEM scale-factor columns (4 per chunk): Q_X, unit, P_X (P8), K and V rings
   // TMEM scale-factor columns (4 per chunk): Q_X, unit, P_X (P8), K and V
   // rings.  A V stage's scales cover its d + 16 rows (row r in column r/32):
   // at d = 64 the ones rows 64..79 fall in the chunk's third column, at
