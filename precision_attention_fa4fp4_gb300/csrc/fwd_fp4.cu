@@ -579,8 +579,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
           sfw |= (uint32_t)(X + 127) << (8 * g);
           uint32_t w[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            w[e] = pack_e4m3x4(s[g][4 * e] * inv, s[g][4 * e + 1] * inv, s[g][4 * e + 2] * inv, s[g][4 * e + 3] * inv);
+          for (int e = 0; e < 8; ++e) {
+            const float2 a = fmul2(make_float2(s[g][4 * e], s[g][4 * e + 1]), make_float2(inv, inv));
+            const float2 b = fmul2(make_float2(s[g][4 * e + 2], s[g][4 * e + 3]), make_float2(inv, inv));
+            w[e] = pack_e4m3x4(a.x, a.y, b.x, b.y);
+          }
           *reinterpret_cast<uint4*>(pb + (((2 * g) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
           *reinterpret_cast<uint4*>(pb + (((2 * g + 1) ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
         }
