@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from gpu_util import assert_close, require_gpu
-from precision_attention_fa4fp4_gb300.inputs import TRAIN_8B, Workload, make_inputs
+from precision_attention_fa4fp4_gb300.inputs import TRAIN_8B, Workload, extreme_logit_inputs, make_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -129,3 +129,25 @@ def test_unit_std_qk(d, qk_std):
     (logits of std ~1 after scaling): more peaked rows, a wider range of P
     and dS inside each MXFP8 block."""
     check(Workload(f"bwd_std{qk_std}_d{d}", 1, 4, 2, 200, d, causal=True, qk_std=qk_std), seed=0)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_extreme_logits(causal):
+    """Scaled logits of several hundred (LSE > 500): the score accumulators
+    start at -LSE log2 e / c of magnitude ~10^4, so their sums cancel to the
+    offset that P is taken from; the gradients must still match the oracle."""
+    fa = require_gpu()
+    q, k, v = extreme_logit_inputs()
+    g = torch.Generator().manual_seed(17)
+    do = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    dq, dk, dv, O, L = gpu_grads(fa, q, k, v, do, causal)
+    assert np.max(L) > 500
+    Q4, K4, V4, Q8, K8, V8 = oracle_views(q, k, v)
+    dQ, dK, dV = oracle.bwd(Q4, K4, Q8, K8, V8, O, do.float().numpy(), L, causal=causal)
+    d = q.shape[-1]
+    for nm, got, want in (("dQ", dq, dQ), ("dK", dk, dK), ("dV", dv, dV)):
+        # K is scaled up to 5x here, so dQ and dK reach ~10^2: the max-abs bar
+        # is taken relative to the largest gradient (rel-L2 as everywhere)
+        want = want.reshape(-1, d)
+        assert_close(got.reshape(-1, d), want, f"extreme logits {nm}",
+                     mabs=1e-2 * max(1.0, float(np.max(np.abs(want)))))
