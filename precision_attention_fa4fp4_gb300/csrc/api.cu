@@ -204,6 +204,7 @@ static fa4fp4_status fwd_common(const void* qc, const void* qs, const void* kc, 
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.Np = Np;
   p.causal = causal ? 1 : 0;
   p.out_bf16 = out_dtype == FA4FP4_OUT_BF16;
+  p.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31) == 0;   // rows are 128 or 256 bytes (bf16) or more
   p.fp8pv = fp8pv;
   p.ts_q = ts_q;
   p.ts_k = ts_k;

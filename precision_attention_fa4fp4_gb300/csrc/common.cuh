@@ -132,6 +132,13 @@ FA4_DEV void tma_reduce_add_3d(const CUtensorMap* map, const void* src_smem, int
       : "memory");
 }
 FA4_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// One 32-byte global store (the address must be 32-byte aligned).
+FA4_DEV void st_global_v8(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
 // the issuing thread's bulk groups have finished reading shared memory
 FA4_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // ... all but the most recent one have

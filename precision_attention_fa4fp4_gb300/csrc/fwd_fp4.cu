@@ -643,25 +643,46 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
         tmem_ld32(lane_base + COL_O0 + L::NO * x + 32 * g, v);
         tmem_ld_wait();
         reg_fence32(v);
+        // each thread writes its own row: 32-byte stores where O is 32-byte
+        // aligned (every row then is), else 16-byte ones
         if (valid && p.out_bf16) {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow + 32 * g);
+          uint32_t w[16];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t w[4];
+          for (int e = 0; e < 16; ++e) {
+            const float2 t = fmul2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])),
+                                   make_float2(inv_l, inv_l));
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(t.x, t.y);
+            w[e] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.o) + orow + 32 * g;
+          if (p.o_align32) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(v[q * 8 + 2 * e]) * inv_l,
-                                                       __uint_as_float(v[q * 8 + 2 * e + 1]) * inv_l);
-              w[e] = *reinterpret_cast<uint32_t*>(&t);
-            }
-            dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int h = 0; h < 2; ++h)
+              st_global_v8(dst + 16 * h, reinterpret_cast<const uint32_t(&)[8]>(w[8 * h]));
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              reinterpret_cast<uint4*>(dst)[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
           }
         } else if (valid) {
-          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + orow + 32 * g);
+          uint32_t w[32];
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv_l, __uint_as_float(v[4 * q + 1]) * inv_l,
-                                 __uint_as_float(v[4 * q + 2]) * inv_l, __uint_as_float(v[4 * q + 3]) * inv_l);
+          for (int e = 0; e < 32; e += 2) {
+            const float2 t = fmul2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                   make_float2(inv_l, inv_l));
+            w[e] = __float_as_uint(t.x);
+            w[e + 1] = __float_as_uint(t.y);
+          }
+          float* dst = reinterpret_cast<float*>(p.o) + orow + 32 * g;
+          if (p.o_align32) {
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+              st_global_v8(dst + 8 * h, reinterpret_cast<const uint32_t(&)[8]>(w[8 * h]));
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              reinterpret_cast<uint4*>(dst)[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+          }
         }
       }
       // LSE: Direct-P codes carry the factor 6 of 6*2^x, the FP8 route does not

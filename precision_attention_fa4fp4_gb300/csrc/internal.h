@@ -48,6 +48,7 @@ struct FwdFp4Params {
   float* lse;
   unsigned* err;
   int B, Hq, Hkv, N, d, Np, causal, out_bf16;
+  int o_align32;                    // O 32-byte aligned: the epilogue writes 32-byte words
   int fp8pv;                        // 0: Direct-P (E2M1 P); 1: FP8 P/V route (E4M3 P and V)
   const float* ts_q;                // NVFP4 Q/K: device tensor scales; nullptr for MXFP4 Q/K
   const float* ts_k;
