@@ -133,8 +133,8 @@ FA4_DEV void tma_reduce_add_3d(const CUtensorMap* map, const void* src_smem, int
 }
 FA4_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
-// One 32-byte global store (the address must be 32-byte aligned).
-FA4_DEV void st_global_v8(void* p, const uint32_t (&w)[8]) {
+// One 32-byte global store of w[0..7] (the address must be 32-byte aligned).
+FA4_DEV void st_global_v8(void* p, const uint32_t* w) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
                "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
                : "memory");

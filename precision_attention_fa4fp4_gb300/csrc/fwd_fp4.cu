@@ -658,7 +658,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
           if (p.o_align32) {
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-              st_global_v8(dst + 16 * h, reinterpret_cast<const uint32_t(&)[8]>(w[8 * h]));
+              st_global_v8(dst + 16 * h, w + 8 * h);
           } else {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -677,7 +677,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_fp4_kernel(const __grid_const
           if (p.o_align32) {
 #pragma unroll
             for (int h = 0; h < 4; ++h)
-              st_global_v8(dst + 8 * h, reinterpret_cast<const uint32_t(&)[8]>(w[8 * h]));
+              st_global_v8(dst + 8 * h, w + 8 * h);
           } else {
 #pragma unroll
             for (int q = 0; q < 8; ++q)
