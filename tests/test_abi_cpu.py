@@ -91,9 +91,16 @@ def test_argument_errors_before_launch(lib):
 
 
 def test_workspace_size(lib):
-    n = lib.fa4fp4_bwd_workspace_bytes(2, 4, 2, 300, 128)
-    rows = 2 * 4 * 300
-    assert n >= rows * 128 + rows * 4 + 2 * 4 * 128 * 384 + rows * 4
+    """The backward's workspace: the dO row view (codes + scales), the dO
+    column view (codes + scales, N padded to 128) and one 16-byte row of
+    accumulator offsets per query row, each piece rounded up to 256 bytes."""
+    up = lambda x: (x + 255) // 256 * 256
+    for B, Hq, Hkv, N, d in ((2, 4, 2, 300, 128), (1, 6, 3, 1, 64), (2, 32, 8, 8192, 128)):
+        rows = B * Hq * N
+        Np = (N + 127) // 128 * 128
+        want = (up(rows * d) + up(rows * d // 32) + up(B * Hq * d * Np) + up(B * Hq * d * Np // 32)
+                + up(rows * 16))
+        assert lib.fa4fp4_bwd_workspace_bytes(B, Hq, Hkv, N, d) == want
     assert lib.fa4fp4_bwd_workspace_bytes(2, 4, 3, 300, 128) == 0
 
 
