@@ -151,3 +151,30 @@ def test_extreme_logits(causal):
         want = want.reshape(-1, d)
         assert_close(got.reshape(-1, d), want, f"extreme logits {nm}",
                      mabs=1e-2 * max(1.0, float(np.max(np.abs(want)))))
+
+
+@pytest.mark.parametrize("d,N,o_bf16", [(128, 300, False), (64, 129, True), (128, 1, False)])
+def test_preprocess_views_match_the_quantizer(d, N, o_bf16):
+    """The two MXFP8 views of dO that the backward's preprocess leaves in its
+    workspace are byte for byte what the quantizer gives for blocks along d
+    and along N (padded tokens included)."""
+    fa = require_gpu()
+    w = Workload(f"prep_d{d}_n{N}", 2, 4, 2, N, d, causal=True, qk_std=d ** -0.25)
+    q, k, v, do = (t.cuda() for t in make_inputs(w, seed=N + d, with_dout=True))
+    q4, k4 = fa.quantize(q), fa.quantize(k)
+    vt = fa.quantize(v, fa.FMT_MXFP4, fa.ALONG_N)
+    q8c, k8c = fa.quantize(q, fa.FMT_MXFP8, fa.ALONG_N), fa.quantize(k, fa.FMT_MXFP8, fa.ALONG_N)
+    v8r = fa.quantize(v, fa.FMT_MXFP8, fa.ALONG_D)
+    o, lse = fa.fwd(q4, k4, vt, causal=True, out_dtype=fa.OUT_BF16 if o_bf16 else fa.OUT_F32)
+    ws = torch.zeros(fa.bwd_workspace_bytes(w.B, w.Hq, w.Hkv, N, d), dtype=torch.uint8, device="cuda")
+    fa.bwd(q4, k4, q8c, k8c, v8r, o, do, lse, causal=True, workspace=ws)
+    torch.cuda.synchronize()
+    fa.sync_status()
+    row = fa.quantize(do, fa.FMT_MXFP8, fa.ALONG_D)
+    col = fa.quantize(do, fa.FMT_MXFP8, fa.ALONG_N)
+    up = lambda x: (x + 255) // 256 * 256
+    off = 0
+    for t in (row.codes, row.scales, col.codes, col.scales):
+        n = t.numel()
+        assert torch.equal(ws[off:off + n], t.reshape(-1).view(torch.uint8)), f"view piece at {off}"
+        off += up(n)
